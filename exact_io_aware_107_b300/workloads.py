@@ -1,0 +1,168 @@
+"""Seeded synthetic inputs for the attention forward workloads.
+
+This module only draws random numbers and rounds them to the storage dtype.
+It holds none of the attention arithmetic, so both the CUDA path (through
+the tests and the bench) and the CPU oracle can read the very same buffers.
+
+Shapes follow the (batch, heads, seq_len, dim) problem statement of
+"Build a FlashAttention kernel from scratch with Python and NumPy"
+(section "Architecture Overview"); the packed variable-length layout is
+(heads, total_tokens, dim) with a cu_seqlens offset vector, the un-padded
+form described in "Flash Attention vs Standard Attention" (section
+"Critical Implementation Details").
+
+Recipes
+-------
+* ``f32_causal_small``: B=2, H=4, N=128, D=64, causal, fp32.  Q, K, V are
+  drawn with the legacy global generator, ``np.random.seed(0)`` then three
+  ``randn`` calls, exactly the call sequence of the first page's "Step 2".
+* ``bf16_*`` dense: ``np.random.default_rng(seed).standard_normal(shape,
+  dtype=float32)`` for Q, K, V in that order (the generator call of
+  "Building a FlashAttention-2 forward kernel in pure NumPy", "Step 5");
+  Q and K are multiplied by ``qk_std`` in fp32; every tensor is then rounded
+  to bfloat16 with round-to-nearest-even.
+* ``bf16_varlen_causal``: ``default_rng(7)``; 16 lengths from
+  ``integers(256, 8193)``, then Q, K, V of shape (H, sum(lengths), D).
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    dtype: str            # "f32" or "bf16"
+    B: int                # batch (number of sequences for varlen)
+    H: int
+    N: int                # seq_len (total tokens for varlen)
+    D: int
+    causal: bool
+    seed: int
+    qk_std: float = 1.0
+    generator: str = "default_rng"   # or "legacy"
+    varlen: Optional[tuple] = None   # sequence lengths for the packed layout
+    len_draw: Optional[tuple] = None  # (nseq, lo, hi) when the lengths came from the same generator
+
+    @property
+    def scale(self) -> float:
+        """Softmax scale 1/sqrt(D), rounded to fp32 so both sides use the same value."""
+        return float(np.float32(1.0 / math.sqrt(self.D)))
+
+    def flops(self) -> float:
+        """Attention-forward FLOPs: 4*N^2*D per (b,h), halved when causal.
+
+        For varlen the sum runs over sequences.  The causal halving is the
+        usual convention (it counts N^2/2 pairs, not N(N+1)/2).
+        """
+        if self.varlen is not None:
+            pairs = sum(L * L for L in self.varlen)
+            f = 4.0 * self.H * pairs * self.D
+        else:
+            f = 4.0 * self.B * self.H * self.N * self.N * self.D
+        return f / 2 if self.causal else f
+
+    def hbm_bytes(self) -> float:
+        """Algorithmic HBM bytes: Q, K, V read once, O and LSE written once."""
+        elt = 2 if self.dtype == "bf16" else 4
+        rows = self.H * self.N if self.varlen is not None else self.B * self.H * self.N
+        return 4.0 * rows * self.D * elt + rows * 4.0
+
+
+def _varlen_lengths(seed: int, nseq: int, lo: int, hi: int) -> tuple:
+    rng = np.random.default_rng(seed)
+    return tuple(int(x) for x in rng.integers(lo, hi + 1, size=nseq))
+
+
+def _mk(name, dtype, B, H, N, D, causal, seed, qk_std=1.0, generator="default_rng", varlen=None,
+        len_draw=None):
+    return Workload(name, dtype, B, H, N, D, causal, seed, qk_std, generator, varlen, len_draw)
+
+
+def _varlen_workload() -> Workload:
+    lens = _varlen_lengths(7, 16, 256, 8192)
+    return _mk("bf16_varlen_causal_h32_d128", "bf16", len(lens), 32, sum(lens), 128, True, 7,
+               varlen=lens, len_draw=(16, 256, 8192))
+
+
+WORKLOADS = {
+    "f32_causal_b2_h4_n128_d64": _mk("f32_causal_b2_h4_n128_d64", "f32", 2, 4, 128, 64, True, 0,
+                                     generator="legacy"),
+    "bf16_b4_h16_n2048_d64": _mk("bf16_b4_h16_n2048_d64", "bf16", 4, 16, 2048, 64, False, 0),
+    "bf16_causal_b2_h32_n8192_d128": _mk("bf16_causal_b2_h32_n8192_d128", "bf16", 2, 32, 8192,
+                                         128, True, 0),
+    "bf16_causal_b1_h16_n32768_d128_peaked": _mk("bf16_causal_b1_h16_n32768_d128_peaked", "bf16",
+                                                 1, 16, 32768, 128, True, 0, qk_std=2.0),
+    "bf16_varlen_causal_h32_d128": _varlen_workload(),
+}
+
+# The workload the throughput line is quoted on (bf16, causal, D=128, N=8192).
+HEADLINE = "bf16_causal_b2_h32_n8192_d128"
+
+
+def custom(dtype="bf16", B=1, H=1, N=128, D=128, causal=True, seed=0, qk_std=1.0,
+           varlen=None, name="custom") -> Workload:
+    """A workload of arbitrary shape drawn with the default_rng recipe."""
+    if varlen is not None:
+        varlen = tuple(int(x) for x in varlen)
+        B, N = len(varlen), int(sum(varlen))
+    return _mk(name, dtype, B, H, N, D, causal, seed, qk_std, "default_rng", varlen)
+
+
+def cu_seqlens_of(lengths) -> np.ndarray:
+    """Offsets [0, L0, L0+L1, ...] as int32 (the packed-sequence index)."""
+    out = np.zeros(len(lengths) + 1, dtype=np.int32)
+    out[1:] = np.cumsum(np.asarray(lengths, dtype=np.int64))
+    return out
+
+
+def _round_bf16(x32: np.ndarray):
+    """fp32 -> bf16 with round-to-nearest-even (torch's conversion)."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x32)).to(torch.bfloat16)
+
+
+def generate(w: Workload, as_torch=True):
+    """Draw Q, K, V for workload ``w`` on the host.
+
+    Returns a dict with ``q``, ``k``, ``v`` as CPU torch tensors in the
+    storage dtype (bf16 or fp32), ``cu_seqlens`` (int32 numpy or None) and
+    ``shape`` (the tensor shape).  The oracle reads the same tensors through
+    :func:`as_f64`.
+    """
+    import torch
+    shape = (w.H, w.N, w.D) if w.varlen is not None else (w.B, w.H, w.N, w.D)
+    if w.generator == "legacy":
+        np.random.seed(w.seed)
+        q = np.random.randn(*shape).astype(np.float32)
+        k = np.random.randn(*shape).astype(np.float32)
+        v = np.random.randn(*shape).astype(np.float32)
+    else:
+        rng = np.random.default_rng(w.seed)
+        if w.len_draw is not None:
+            # the lengths were drawn first from the same generator
+            nseq, lo, hi = w.len_draw
+            rng.integers(lo, hi + 1, size=nseq)
+        q = rng.standard_normal(shape, dtype=np.float32)
+        k = rng.standard_normal(shape, dtype=np.float32)
+        v = rng.standard_normal(shape, dtype=np.float32)
+    if w.qk_std != 1.0:
+        q *= np.float32(w.qk_std)
+        k *= np.float32(w.qk_std)
+    if w.dtype == "bf16":
+        tq, tk, tv = _round_bf16(q), _round_bf16(k), _round_bf16(v)
+    else:
+        tq, tk, tv = (torch.from_numpy(np.ascontiguousarray(a)) for a in (q, k, v))
+    cu = cu_seqlens_of(w.varlen) if w.varlen is not None else None
+    return {"q": tq, "k": tk, "v": tv, "cu_seqlens": cu, "shape": shape}
+
+
+def as_f64(t) -> np.ndarray:
+    """Exact widening of a CPU torch tensor (bf16 or fp32) to a float64 array."""
+    import torch
+    return t.detach().to("cpu").to(torch.float32).numpy().astype(np.float64)

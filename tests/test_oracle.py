@@ -1,0 +1,313 @@
+"""Pins for the fp64 oracle: closed forms, invariants and brute force.
+
+Each check fixes the oracle against something other than itself, so that a
+plausible slip (a dropped scale, a causal mask that drops or flips the
+diagonal, a transposed operand, a wrong log base, a missing max shift, an
+off-by-one in the slab loop) fails at least one of them.  ``test_mutants_are_caught``
+plants exactly those slips in copies of the oracle and checks that the pins
+reject every one.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import exact as A
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand(rng, *shape, std=1.0):
+    return rng.standard_normal(shape) * std
+
+
+# ---------------------------------------------------------------------------
+# Individual pins, written as functions of an attention implementation so the
+# same checks can be run against planted mistakes.
+# ---------------------------------------------------------------------------
+
+def pin_golden(fn):
+    """Hand-derived three-token example with rational probabilities."""
+    fx = json.load(open(os.path.join(GOLDEN, "closed_form_n3_d2.json")))
+    q, k, v = (np.array(fx[n]) for n in ("q", "k", "v"))
+    for causal, key in ((True, "causal"), (False, "noncausal")):
+        o, lse = fn(q, k, v, fx["scale"], causal)
+        np.testing.assert_allclose(o, np.array(fx[key]["o"]), rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse, np.array(fx[key]["lse"]), rtol=0, atol=1e-14)
+
+
+def pin_brute_force(fn):
+    """Scalar loops with math.exp / math.fsum on tiny shapes, independent of numpy BLAS."""
+    rng = np.random.default_rng(11)
+    for n in (1, 2, 3, 5, 8):
+        for d in (1, 2, 4):
+            q, k, v = _rand(rng, n, d), _rand(rng, n, d), _rand(rng, n, d)
+            scale = 0.7
+            for causal in (False, True):
+                o, lse = fn(q, k, v, scale, causal)
+                for i in range(n):
+                    keys = range(i + 1) if causal else range(n)
+                    s = [scale * math.fsum(q[i, t] * k[j, t] for t in range(d)) for j in keys]
+                    mx = max(s)
+                    e = [math.exp(x - mx) for x in s]
+                    den = math.fsum(e)
+                    for t in range(d):
+                        ref = math.fsum(e[c] * v[j, t] for c, j in enumerate(keys)) / den
+                        assert abs(o[i, t] - ref) <= 1e-13 * (1 + abs(ref)), (n, d, causal, i, t)
+                    assert abs(lse[i] - (mx + math.log(den))) <= 1e-13 * (1 + abs(mx)), (n, d, i)
+
+
+def pin_causal_row0(fn):
+    """Causal row 0 sees only key 0: O_0 = V_0, LSE_0 = scale * q_0 . k_0."""
+    rng = np.random.default_rng(3)
+    q, k, v = _rand(rng, 40, 16), _rand(rng, 40, 16), _rand(rng, 40, 16)
+    o, lse = fn(q, k, v, 0.25, True)
+    np.testing.assert_array_equal(o[0], v[0])
+    assert abs(lse[0] - 0.25 * math.fsum(q[0] * k[0])) < 1e-14
+
+
+def pin_zero_query(fn):
+    """Q = 0 makes every allowed score 0: O is the (prefix) mean of V, LSE = ln(count)."""
+    rng = np.random.default_rng(4)
+    n, d = 37, 8
+    q = np.zeros((n, d))
+    k, v = _rand(rng, n, d), _rand(rng, n, d)
+    o, lse = fn(q, k, v, 0.3, True)
+    counts = np.arange(1, n + 1)[:, None]
+    np.testing.assert_allclose(o, np.cumsum(v, axis=0) / counts, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, np.log(np.arange(1, n + 1)), rtol=0, atol=1e-14)
+    o, lse = fn(q, k, v, 0.3, False)
+    np.testing.assert_allclose(o, np.broadcast_to(v.mean(axis=0), o.shape), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, np.full(n, math.log(n)), rtol=0, atol=1e-14)
+
+
+def pin_value_ones(fn):
+    rng = np.random.default_rng(5)
+    q, k = _rand(rng, 33, 8), _rand(rng, 33, 8)
+    for causal in (False, True):
+        o, _ = fn(q, k, np.ones((33, 8)), 0.5, causal)
+        np.testing.assert_allclose(o, 1.0, rtol=0, atol=1e-14)
+
+
+def pin_permutation(fn):
+    """Non-causal: permuting K and V rows together changes nothing."""
+    rng = np.random.default_rng(6)
+    q, k, v = _rand(rng, 29, 8), _rand(rng, 29, 8), _rand(rng, 29, 8)
+    perm = rng.permutation(29)
+    o1, l1 = fn(q, k, v, 0.4, False)
+    o2, l2 = fn(q, k[perm], v[perm], 0.4, False)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+def pin_key_shift(fn):
+    """K_j -> K_j + u: every score of row i moves by scale*q_i.u, so O is unchanged
+    and LSE_i moves by exactly that amount (the softmax shift invariance)."""
+    rng = np.random.default_rng(7)
+    q, k, v = _rand(rng, 31, 8), _rand(rng, 31, 8), _rand(rng, 31, 8)
+    u = _rand(rng, 8)
+    for causal in (False, True):
+        o1, l1 = fn(q, k, v, 0.35, causal)
+        o2, l2 = fn(q, k + u, v, 0.35, causal)
+        np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(l2 - l1, 0.35 * (q @ u), rtol=0, atol=1e-12)
+
+
+def pin_causality(fn):
+    """Causal: changing keys/values j > i leaves row i untouched (bit for bit)."""
+    rng = np.random.default_rng(8)
+    n = 50
+    q, k, v = _rand(rng, n, 8), _rand(rng, n, 8), _rand(rng, n, 8)
+    o1, l1 = fn(q, k, v, 0.3, True)
+    i = 20
+    k2, v2 = k.copy(), v.copy()
+    k2[i + 1:] = _rand(rng, n - i - 1, 8) * 5
+    v2[i + 1:] = _rand(rng, n - i - 1, 8) * 5
+    o2, l2 = fn(q, k2, v2, 0.3, True)
+    np.testing.assert_allclose(o1[:i + 1], o2[:i + 1], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(l1[:i + 1], l2[:i + 1], rtol=0, atol=1e-14)
+    assert np.abs(o1[i + 1:] - o2[i + 1:]).max() > 1e-3
+
+
+def pin_large_scores(fn):
+    """Scores near +-700 overflow exp unless the row max is subtracted first."""
+    rng = np.random.default_rng(9)
+    q, k, v = _rand(rng, 16, 4), _rand(rng, 16, 4), _rand(rng, 16, 4)
+    o1, l1 = fn(q, k, v, 0.5, False)
+    q2 = q * 400.0
+    o2, l2 = fn(q2, k, v, 0.5 / 400.0, False)      # identical scores, bigger operands
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    big = np.zeros((16, 4))
+    big[:, 0] = 900.0
+    kk = np.ones((16, 4))
+    o3, l3 = fn(big, kk, v, 1.0, False)            # every score 900: uniform weights
+    assert np.all(np.isfinite(o3)) and np.all(np.isfinite(l3))
+    np.testing.assert_allclose(o3, np.broadcast_to(v.mean(axis=0), o3.shape), atol=1e-12)
+    np.testing.assert_allclose(l3, 900.0 + math.log(16), rtol=0, atol=1e-10)
+
+
+ALL_PINS = [pin_golden, pin_brute_force, pin_causal_row0, pin_zero_query, pin_value_ones,
+            pin_permutation, pin_key_shift, pin_causality, pin_large_scores]
+
+
+def _oracle_plane(q, k, v, scale, causal):
+    return A.attention_plane(q, k, v, scale, causal)
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=lambda p: p.__name__)
+def test_oracle_pins(pin):
+    pin(_oracle_plane)
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=lambda p: p.__name__)
+def test_online_tiled_pins(pin):
+    pin(lambda q, k, v, s, c: A.online_tiled(q, k, v, s, c, br=4, bc=3))
+
+
+# ---------------------------------------------------------------------------
+# Structural checks of the oracle's own code paths
+# ---------------------------------------------------------------------------
+
+def test_softmax_rows_sum_to_one():
+    rng = np.random.default_rng(1)
+    for causal in (False, True):
+        p = A.softmax_probs(_rand(rng, 70, 16), _rand(rng, 70, 16), 0.25, causal)
+        np.testing.assert_allclose(p.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+        if causal:
+            assert np.all(np.triu(p, 1) == 0.0)
+            assert np.all(np.diag(p) > 0)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 17, 128, 129, 300])
+@pytest.mark.parametrize("tile", [1, 16, 32, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_online_tiled_equals_materialised(n, tile, causal):
+    if tile == 1 and n > 129:
+        pytest.skip("tile 1 at n=300 is slow and adds nothing")
+    rng = np.random.default_rng(n * 7 + tile)
+    q, k, v = _rand(rng, n, 16), _rand(rng, n, 16), _rand(rng, n, 16)
+    o1, l1 = A.attention_plane(q, k, v, 0.25, causal)
+    o2, l2 = A.online_tiled(q, k, v, 0.25, causal, br=tile, bc=tile)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-12)
+
+
+def test_slab_path_equals_full_matrix(monkeypatch):
+    rng = np.random.default_rng(2)
+    n = 1100
+    q, k, v = _rand(rng, n, 8), _rand(rng, n, 8), _rand(rng, n, 8)
+    for causal in (False, True):
+        o1, l1 = A.attention_plane(q, k, v, 0.3, causal)
+        monkeypatch.setattr(A, "FULL_MATRIX_MAX_N", 100)
+        monkeypatch.setattr(A, "SLAB_ROWS", 97)        # ragged slabs
+        o2, l2 = A.attention_plane(q, k, v, 0.3, causal)
+        monkeypatch.undo()
+        np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+def test_attention_rows_equal_plane():
+    rng = np.random.default_rng(12)
+    n = 300
+    q, k, v = _rand(rng, n, 8), _rand(rng, n, 8), _rand(rng, n, 8)
+    rows = [0, 1, 127, 128, 129, 299]
+    for causal in (False, True):
+        o, l = A.attention_plane(q, k, v, 0.3, causal)
+        o2, l2 = A.attention_rows(q, k, v, 0.3, causal, rows)
+        np.testing.assert_allclose(o[rows], o2, rtol=0, atol=1e-14)
+        np.testing.assert_allclose(l[rows], l2, rtol=0, atol=1e-14)
+
+
+def test_varlen_equals_per_sequence_dense():
+    rng = np.random.default_rng(13)
+    lens = [1, 5, 130, 64]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    H, D = 3, 8
+    q, k, v = (_rand(rng, H, cu[-1], D) for _ in range(3))
+    o, lse = A.attention(q, k, v, 0.3, True, cu_seqlens=cu)
+    for s in range(len(lens)):
+        a, e = cu[s], cu[s + 1]
+        od, ld = A.attention(q[None, :, a:e], k[None, :, a:e], v[None, :, a:e], 0.3, True)
+        np.testing.assert_array_equal(o[:, a:e], od[0])
+        np.testing.assert_array_equal(lse[:, a:e], ld[0])
+        # first row of each sequence is its own first value row
+        np.testing.assert_array_equal(o[:, a], v[:, a])
+
+
+def test_dense_batch_layout():
+    rng = np.random.default_rng(14)
+    q, k, v = (_rand(rng, 2, 3, 20, 4) for _ in range(3))
+    o, lse = A.attention(q, k, v, 0.5, True)
+    assert o.shape == (2, 3, 20, 4) and lse.shape == (2, 3, 20)
+    for b in range(2):
+        for h in range(3):
+            op, lp = A.attention_plane(q[b, h], k[b, h], v[b, h], 0.5, True)
+            np.testing.assert_array_equal(o[b, h], op)
+            np.testing.assert_array_equal(lse[b, h], lp)
+
+
+def test_single_token_closed_form():
+    rng = np.random.default_rng(15)
+    q, k, v = _rand(rng, 1, 8), _rand(rng, 1, 8), _rand(rng, 1, 8)
+    for causal in (False, True):
+        o, lse = A.attention_plane(q, k, v, 0.125, causal)
+        np.testing.assert_array_equal(o[0], v[0])
+        assert abs(lse[0] - 0.125 * math.fsum(q[0] * k[0])) < 1e-15
+
+
+# ---------------------------------------------------------------------------
+# Planted mistakes: each mutant must fail at least one pin.
+# ---------------------------------------------------------------------------
+
+def _mutant(kind):
+    def fn(q, k, v, scale, causal):
+        q, k, v = (np.asarray(a, dtype=np.float64) for a in (q, k, v))
+        n = q.shape[0]
+        sc = 1.0 if kind == "no_scale" else scale
+        s = sc * (q @ k.T) if kind != "transpose" else sc * (k @ q.T)
+        i = np.arange(n)[:, None]
+        j = np.arange(n)[None, :]
+        if causal:
+            keep = {"no_diag": j < i, "flipped": j >= i}.get(kind, j <= i)
+            if kind == "no_diag":
+                keep = keep | ((i == 0) & (j == 0))      # keep row 0 defined
+            s = np.where(keep, s, -np.inf)
+        m = s.max(axis=1, keepdims=True)
+        if kind == "no_max":
+            m = np.zeros_like(m)
+        e = np.exp(s - m)
+        l = e.sum(axis=1, keepdims=True)
+        o = (e / l) @ v
+        if kind == "value_transpose":
+            o = (e / l) @ v[::-1]
+        lse = m[:, 0] + (np.log2(l[:, 0]) if kind == "log2" else np.log(l[:, 0]))
+        if kind == "lse_no_max":
+            lse = np.log(l[:, 0])
+        return o, lse
+    return fn
+
+
+MUTANTS = ["no_scale", "transpose", "no_diag", "flipped", "no_max", "value_transpose", "log2",
+           "lse_no_max"]
+
+
+def test_reference_implementation_of_mutant_harness_passes():
+    # the harness itself, with no mistake planted, passes every pin
+    for pin in ALL_PINS:
+        pin(_mutant("none"))
+
+
+@pytest.mark.parametrize("kind", MUTANTS)
+def test_mutants_are_caught(kind):
+    fn = _mutant(kind)
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(fn)
+        except (AssertionError, FloatingPointError, ValueError):
+            failed.append(pin.__name__)
+    assert failed, f"mutant {kind} passed every pin"
