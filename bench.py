@@ -1,0 +1,385 @@
+"""Throughput of the exact attention forward on B300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+A step is one attention forward over the whole workload (default: bf16,
+causal, B=2, H=32, N=8192, D=128).  ``value`` is device-timed TFLOP/s with
+inputs resident in HBM (CUDA events on the launching stream, K back-to-back
+launches; the inputs, 403 MB, exceed the 126 MB L2 so no flush is needed).
+``e2e`` is the same metric through the same C-ABI call with pinned host
+buffers: every step copies Q, K, V host->device and O, LSE device->host inside
+the timed region.  Under torchrun each rank runs its own replica of the
+workload (weak scaling); the slowest rank's time is used.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead,
+each step on a bounded sample of the same workload (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from exact_io_aware_107_b300 import workloads as W  # noqa: E402
+
+METRIC = "attention fwd TFLOPS (bf16, causal) and % of B300 dense bf16 tensor peak"
+KERNEL_SOURCES = ["exact_io_aware_107_b300/csrc/fwd_bf16_sm103.cuh",
+                  "exact_io_aware_107_b300/csrc/ptx.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("bf16_tflops", 1800.0), d.get("hbm_gbs", 6400.0), "measured"
+    return 1800.0, 6400.0, "fallback"
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per launch from an ncu capture, if taken on the current kernel source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    d = json.load(open(TRAFFIC_FILE))
+    e = d.get(workload)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_rows_sample(w, x, plane_index: int, rows: np.ndarray, threads: int):
+    """Run the oracle on the given rows of one plane; returns (flops, seconds)."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    b, h = divmod(plane_index, w.H)
+    q = W.as_f64(x["q"][b, h])
+    k = W.as_f64(x["k"][b, h])
+    v = W.as_f64(x["v"][b, h])
+    from threadpoolctl import threadpool_limits
+    chunks = [c for c in np.array_split(rows, max(1, threads)) if len(c)]
+    with threadpool_limits(limits=1):
+        t0 = time.perf_counter()
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda r: oracle.attention_rows(q, k, v, w.scale, w.causal, r), chunks))
+        dt = time.perf_counter() - t0
+    keys = (rows + 1) if w.causal else np.full(len(rows), w.N)
+    flops = float(4.0 * w.D * keys.sum())
+    return flops, dt
+
+
+def cpu_baseline(w, x, budget_s: float = 12.0):
+    """Oracle throughput on a bounded sample: the last rows of plane 0 (full-length causal rows)."""
+    threads = host_cores()
+    n_rows = 256
+    flops_total, t_total, rows_done = 0.0, 0.0, 0
+    while t_total < budget_s and rows_done < w.N:
+        r1 = w.N - rows_done
+        rows = np.arange(max(0, r1 - n_rows), r1)
+        f, dt = oracle_rows_sample(w, x, 0, rows, threads)
+        flops_total += f
+        t_total += dt
+        rows_done += len(rows)
+        n_rows = min(4096, n_rows * 2)
+    return {"value": flops_total / t_total / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"fp64 oracle on the last {rows_done} query rows of plane (b=0,h=0) "
+                      f"of {w.name} ({t_total:.1f} s of CPU work, {threads} threads)"}
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    x = W.generate(w)
+    threads = host_cores()
+    rows = np.arange(w.N - 512, w.N)        # one step: 512 full-length rows of plane 0
+    for _ in range(args.warmup):
+        oracle_rows_sample(w, x, 0, rows, threads)
+    flops = secs = 0.0
+    for _ in range(args.steps):
+        f, dt = oracle_rows_sample(w, x, 0, rows, threads)
+        flops += f
+        secs += dt
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: fp64 oracle on query rows {w.N - 512}..{w.N - 1} "
+                                   f"of plane (b=0,h=0) of {w.name}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(w):
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
+           "dtype_in": w.dtype, "flops_per_step": w.flops(),
+           "l2": "inputs larger than L2 (no flush)" if 3 * w.hbm_bytes() / 4 > 126e6
+           else "L2 flushed between steps"}
+    if w.varlen is not None:
+        cfg["seq_lens"] = list(w.varlen)
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# CUDA path
+# ---------------------------------------------------------------------------
+
+def run_ours(args, w):
+    import torch
+    from exact_io_aware_107_b300 import _binding, attention_forward, device_error
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    _binding.load()
+    x = W.generate(w)
+    dev = torch.device("cuda", local)
+    q, k, v = (t.to(dev) for t in (x["q"], x["k"], x["v"]))
+    cu = None if x["cu_seqlens"] is None else torch.as_tensor(x["cu_seqlens"]).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = None
+    if 3 * w.hbm_bytes() / 4 <= 126e6:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        if flush is not None:
+            flush.zero_()
+        attention_forward(q, k, v, causal=w.causal, scale=w.scale, cu_seqlens=cu, out=o, lse=lse,
+                          stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    # --- device-timed region (inputs resident) ---
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            starts[i].record(stream)
+            attention_forward(q, k, v, causal=w.causal, scale=w.scale, cu_seqlens=cu, out=o,
+                              lse=lse, stream=stream)
+            ends[i].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    if device_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_ms = sum(launch_ms) / len(launch_ms)
+    ms_step = max_over_ranks(total_ms / args.steps, ws)
+    flops = w.flops()
+    value = ws * flops / (ms_step * 1e-3) / 1e12
+
+    # --- end-to-end region: pinned host buffers, copies inside the timed region ---
+    hq, hk, hv = (t.pin_memory() for t in (x["q"], x["k"], x["v"]))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        q.copy_(hq, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        attention_forward(q, k, v, causal=w.causal, scale=w.scale, cu_seqlens=cu, out=o, lse=lse,
+                          stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, ws)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    peak_tf, _, peak_kind = load_peaks()
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(w),
+        "pct_of_peak": 100.0 * value / ws / peak_tf,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": achieved / peak_tf,
+                     "peak_source": f"{peak_kind} cuBLAS bf16 burst (MEASURED_PEAKS.json)"
+                     if peak_kind == "measured" else "fallback 1.8 PFLOP/s",
+                     "kernel": f"attn_fwd_bf16_kernel<{w.D}>",
+                     "traffic": measured_traffic(w.name),
+                     "algorithmic_bytes": w.hbm_bytes()},
+        "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "gpu": torch.cuda.get_device_name(dev),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, x)
+    if rank == 0:
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,281 @@
+// C ABI of the attention forward: argument checks, TMA descriptors, launches.
+//
+// One translation unit holds the device error word and every kernel, so the
+// library needs no relocatable device code.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn_b300.h"
+#include "fwd_bf16_sm103.cuh"
+#include "fwd_f32.cuh"
+#include "ptx.cuh"
+
+namespace attn {
+
+__device__ unsigned int g_dev_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<unsigned long long> g_timeout_ns{1000000000ull};
+
+struct DeviceState {
+  int checked = 0;  // 0 unknown, 1 ok, -1 wrong arch
+  unsigned int* err = nullptr;
+  bool attrs_set = false;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Checks the current device once and fetches what the launches need.
+int prepare_device(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (st.checked == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_LAUNCH;
+    }
+    if (major != 10 || minor != 3) {
+      st.checked = -1;
+    } else {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_dev_error) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH;
+      }
+      st.err = static_cast<unsigned int*>(p);
+      if (g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr) {
+          cudaGetLastError();
+          return ATTN_ERR_LAUNCH;
+        }
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+      }
+      st.checked = 1;
+    }
+  }
+  if (st.checked < 0) return ATTN_ERR_ARCH;
+  if (!st.attrs_set) {
+    if (cudaFuncSetAttribute(attn_fwd_bf16_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Bf16Cfg<64>::SMEM_ALLOC) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_fwd_bf16_kernel<128>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Bf16Cfg<128>::SMEM_ALLOC) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_LAUNCH;
+    }
+    const int f32_smem = (2 * kF32BM * 128 + kF32BN * 129) * 4;
+    if (cudaFuncSetAttribute(attn_fwd_f32_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             f32_smem) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_LAUNCH;
+    }
+    st.attrs_set = true;
+  }
+  *out = &st;
+  return ATTN_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shared argument checks of both entry points.
+int check_common(const void* q, const void* k, const void* v, const void* o, const void* lse,
+                 int B, int H, int N, int D, const int* cu_seqlens, float scale) {
+  if (B < 1 || H < 1 || N < 0) return ATTN_ERR_SHAPE;
+  if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_SCALE;
+  if (N == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4))
+    return ATTN_ERR_ALIGN;
+  if (cu_seqlens && !aligned(cu_seqlens, 4)) return ATTN_ERR_ALIGN;
+  // element counts must fit the 64-bit offsets and the int row indices
+  const long long planes = cu_seqlens ? static_cast<long long>(H) : 1LL * B * H;
+  if (planes > (1LL << 31) - 1) return ATTN_ERR_SHAPE;
+  if (planes * N > (1LL << 40)) return ATTN_ERR_SHAPE;
+  (void)D;
+  return ATTN_OK;
+}
+
+int encode_bf16_map(CUtensorMap* map, const void* base, int D, int rows, int planes) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(planes)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(rows) * D * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+__global__ void wait_selftest_kernel(unsigned long long budget, unsigned int* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const WaitCtl ctl{&abort_flag, err, budget};
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, ctl);  // nothing ever arrives
+  __syncthreads();
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int N, int D, const int* cu_seqlens, int causal, float scale,
+                        void* stream) {
+  int rc = check_common(q, k, v, o, lse, B, H, N, D, cu_seqlens, scale);
+  if (rc != ATTN_OK) return rc;
+  if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+  if (N == 0) return ATTN_OK;
+  DeviceState* st = nullptr;
+  rc = prepare_device(&st);
+  if (rc != ATTN_OK) return rc;
+
+  const int planes = cu_seqlens ? H : B * H;
+  CUtensorMap mq, mk, mv;
+  if (encode_bf16_map(&mq, q, D, N, planes) != ATTN_OK ||
+      encode_bf16_map(&mk, k, D, N, planes) != ATTN_OK ||
+      encode_bf16_map(&mv, v, D, N, planes) != ATTN_OK)
+    return ATTN_ERR_LAUNCH;
+
+  Bf16Params p;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.cu_seqlens = cu_seqlens;
+  p.nseq = cu_seqlens ? B : 0;
+  p.planes = planes;
+  p.rows = N;
+  p.n_qblk = cu_seqlens ? (N / 256 + B) : (N + 255) / 256;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = g_timeout_ns.load();
+  p.err = st->err;
+
+  const long long grid = 1LL * p.n_qblk * planes;
+  if (grid > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (D == 64)
+    attn_fwd_bf16_kernel<64><<<static_cast<unsigned>(grid), Bf16Cfg<64>::THREADS,
+                               Bf16Cfg<64>::SMEM_ALLOC, s>>>(mq, mk, mv, p);
+  else
+    attn_fwd_bf16_kernel<128><<<static_cast<unsigned>(grid), Bf16Cfg<128>::THREADS,
+                                Bf16Cfg<128>::SMEM_ALLOC, s>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+extern "C" int attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                            int B, int H, int N, int D, const int* cu_seqlens, int causal,
+                            float scale, void* stream) {
+  int rc = check_common(q, k, v, o, lse, B, H, N, D, cu_seqlens, scale);
+  if (rc != ATTN_OK) return rc;
+  if (D < 1 || D > 128) return ATTN_ERR_HEADDIM;
+  if (N == 0) return ATTN_OK;
+  DeviceState* st = nullptr;
+  rc = prepare_device(&st);
+  if (rc != ATTN_OK) return rc;
+
+  F32Params p;
+  p.o = o;
+  p.lse = lse;
+  p.cu_seqlens = cu_seqlens;
+  p.nseq = cu_seqlens ? B : 0;
+  p.planes = cu_seqlens ? H : B * H;
+  p.rows = N;
+  p.n_qblk = cu_seqlens ? (N / kF32BM + B) : (N + kF32BM - 1) / kF32BM;
+  p.D = D;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.err = st->err;
+  const long long grid = 1LL * p.n_qblk * p.planes;
+  if (grid > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  const int smem = (2 * kF32BM * D + kF32BN * (D + 1)) * 4;
+  attn_fwd_f32_kernel<4><<<static_cast<unsigned>(grid), 128, smem,
+                           static_cast<cudaStream_t>(stream)>>>(q, k, v, p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+extern "C" const char* attn_strerror(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_NULL: return "a required pointer is NULL";
+    case ATTN_ERR_SHAPE: return "invalid shape (B, H >= 1, N >= 0, sizes within index range)";
+    case ATTN_ERR_HEADDIM: return "head dimension not supported by this entry point";
+    case ATTN_ERR_ALIGN: return "tensor pointers must be 16-byte aligned (lse, cu_seqlens 4-byte)";
+    case ATTN_ERR_ARCH: return "current device is not compute capability 10.3 (sm_103a)";
+    case ATTN_ERR_LAUNCH: return "CUDA runtime error during set-up or launch";
+    case ATTN_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out of time";
+    case ATTN_ERR_BOUNDS: return "cu_seqlens entries outside [0, N] or decreasing";
+    case ATTN_ERR_SCALE: return "scale must be finite and > 0";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int attn_get_device_error(void* stream) {
+  DeviceState* st = nullptr;
+  int rc = prepare_device(&st);
+  if (rc != ATTN_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned int v = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess ||
+      cudaMemcpyFromSymbolAsync(&v, g_dev_error, sizeof(v), 0, cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaMemsetAsync(st->err, 0, sizeof(unsigned int), s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  if (v & kDevErrTimeout) return ATTN_ERR_TIMEOUT;
+  if (v & kDevErrBounds) return ATTN_ERR_BOUNDS;
+  return ATTN_OK;
+}
+
+extern "C" int attn_set_wait_timeout_ns(unsigned long long ns) {
+  if (ns == 0) return ATTN_ERR_SHAPE;
+  g_timeout_ns.store(ns);
+  return ATTN_OK;
+}
+
+extern "C" int attn_wait_selftest(unsigned long long timeout_ns, void* stream) {
+  if (timeout_ns == 0) return ATTN_ERR_SHAPE;
+  DeviceState* st = nullptr;
+  int rc = prepare_device(&st);
+  if (rc != ATTN_OK) return rc;
+  wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(timeout_ns, st->err);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+extern "C" int attn_version(void) { return 100; }

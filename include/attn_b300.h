@@ -1,0 +1,124 @@
+/*
+ * attn_b300.h - C ABI of the exact IO-aware attention forward for B300 (sm_103a).
+ *
+ * The operation is the exact scaled-dot-product attention forward
+ *
+ *     O     = softmax(scale * Q K^T + causal mask) V
+ *     LSE_i = ln sum_{j allowed for i} exp(scale * q_i . k_j)
+ *
+ * over the (batch, heads, seq_len, dim) problem statement of "Build a
+ * FlashAttention kernel from scratch with Python and NumPy" (section
+ * "Architecture Overview"), computed tile by tile with the online-softmax
+ * update of "Building a FlashAttention-2 forward kernel in pure NumPy"
+ * (sections "Architecture Overview" and "Step 3: Online softmax core") so
+ * that the N x N score matrix never exists in memory.  The causal mask keeps
+ * key j for query i when j <= i (the diagonal is kept, as the comment of the
+ * first page's "Step 3" states).  LSE is the natural log of the sum of
+ * exponentials of the scaled, masked scores: with the running max m and
+ * running sum l of the FA-2 page's invariant, LSE = m + ln l.
+ *
+ * Layouts (all tensors row-major and contiguous, the contiguity that
+ * "Flash Attention vs Standard Attention" asks of its inputs):
+ *   dense  (cu_seqlens == NULL): q, k, v, o are (B, H, N, D); lse is (B, H, N).
+ *   packed (cu_seqlens != NULL): the un-padded variable-length form of
+ *          "Flash Attention vs Standard Attention" ("Critical Implementation
+ *          Details"): B is the number of sequences and N the total token
+ *          count; q, k, v, o are (H, N, D) and lse is (H, N).  cu_seqlens is
+ *          a DEVICE int32 array of B+1 offsets; sequence s occupies tokens
+ *          [cu_seqlens[s], cu_seqlens[s+1]).  Each sequence attends only to
+ *          itself; causal positions are relative to the sequence start.
+ *
+ * Ownership and synchrony: every pointer is caller-owned device memory.  The
+ * library allocates no device memory per call, keeps no pointer after a call
+ * returns, and never synchronises the host: work is enqueued on `stream`
+ * (a cudaStream_t; NULL means the legacy default stream) and the call
+ * returns.  The host never reads cu_seqlens, so the grid is sized from N and
+ * B and surplus CTAs exit at once.
+ *
+ * Errors: argument problems are reported synchronously by the return value
+ * and nothing is launched.  Problems only the device can see (a wait that ran
+ * out of time, cu_seqlens entries outside [0, N] or decreasing) set bits in a
+ * per-device error word that attn_get_device_error() reads and clears; the
+ * affected CTAs stop early and leave their outputs unwritten.  N == 0 is a
+ * no-op that returns ATTN_OK.
+ *
+ * Thread safety: calls on distinct streams may come from distinct threads.
+ */
+#ifndef ATTN_B300_H
+#define ATTN_B300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_NULL = -1,     /* a required pointer is NULL                                */
+  ATTN_ERR_SHAPE = -2,    /* B < 1, H < 1, N < 0, or sizes overflow the index types    */
+  ATTN_ERR_HEADDIM = -3,  /* D not supported by this entry point                       */
+  ATTN_ERR_ALIGN = -4,    /* q/k/v/o not 16-byte aligned, lse/cu_seqlens not 4-byte     */
+  ATTN_ERR_ARCH = -5,     /* current device is not compute capability 10.3             */
+  ATTN_ERR_LAUNCH = -6,   /* the CUDA runtime refused the launch or set-up              */
+  ATTN_ERR_TIMEOUT = -7,  /* (device) a bounded wait inside a kernel ran out of time    */
+  ATTN_ERR_BOUNDS = -8,   /* (device) cu_seqlens entries outside [0, N] or decreasing   */
+  ATTN_ERR_SCALE = -9     /* scale is not a finite number > 0                           */
+} attn_status;
+
+/*
+ * bf16 forward on tcgen05 tensor cores.
+ *   q, k, v : const bf16 (__nv_bfloat16) device pointers, 16-byte aligned.
+ *   o       : bf16 device output, same shape as q, 16-byte aligned.
+ *   lse     : fp32 device output, natural log, 4-byte aligned.
+ *   D       : 64 or 128.
+ *   causal  : 0 or 1 (any non-zero value means 1).
+ *   scale   : softmax scale (1/sqrt(D) in the usual case), finite and > 0.
+ * Arithmetic: bf16 operands, fp32 accumulation of both products, fp32
+ * softmax in base 2; the probabilities are rounded to bf16 for the second
+ * product; O is rounded to bf16 once at the end.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int N, int D, const int* cu_seqlens, int causal, float scale, void* stream);
+
+/*
+ * fp32 forward on CUDA cores: same arguments and layouts with float tensors
+ * (16-byte aligned), 1 <= D <= 128.  Scores, probabilities and accumulators
+ * stay in fp32; exponentials use the accurate expf.
+ */
+int attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
+                 int H, int N, int D, const int* cu_seqlens, int causal, float scale,
+                 void* stream);
+
+/* Static description of a status code. */
+const char* attn_strerror(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (takes precedence) or
+ * ATTN_ERR_BOUNDS; ATTN_ERR_LAUNCH if the synchronisation itself failed.
+ */
+int attn_get_device_error(void* stream);
+
+/*
+ * Budget, in nanoseconds of GPU global time, of every bounded wait inside
+ * the kernels launched after this call (default 1e9 = one second).  Returns
+ * ATTN_ERR_SHAPE for 0.
+ */
+int attn_set_wait_timeout_ns(unsigned long long ns);
+
+/*
+ * Launches one CTA that waits on an mbarrier no thread ever arrives on, with
+ * the given budget, through the same bounded-wait routine the attention
+ * kernels use.  The wait gives up, records ATTN_ERR_TIMEOUT in the device
+ * error word and the kernel returns; nothing traps and the context stays
+ * usable.  Asynchronous like the other calls.
+ */
+int attn_wait_selftest(unsigned long long timeout_ns, void* stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_B300_H */

@@ -1,0 +1,34 @@
+"""Helpers shared by the GPU tests: run the CUDA path, run the oracle, compare."""
+
+import numpy as np
+
+# Tolerances (max absolute error against the fp64 oracle on the same inputs).
+F32_TOL_O = 1e-4
+F32_TOL_LSE = 1e-4
+BF16_TOL_O = 2e-2
+BF16_TOL_LSE = 1e-3
+
+
+def run_cuda(q, k, v, causal, scale, cu_seqlens=None, poison=True):
+    """Run the CUDA path on host tensors; returns fp64 numpy O and LSE."""
+    import torch
+    from exact_io_aware_107_b300 import attention_forward, device_error
+    dq, dk, dv = (t.to("cuda") for t in (q, k, v))
+    dcu = None if cu_seqlens is None else torch.as_tensor(cu_seqlens, dtype=torch.int32).cuda()
+    o = torch.empty_like(dq)
+    lse = torch.empty(dq.shape[:-1], dtype=torch.float32, device="cuda")
+    if poison:
+        o.fill_(float("nan"))
+        lse.fill_(float("nan"))
+    attention_forward(dq, dk, dv, causal=causal, scale=scale, cu_seqlens=dcu, out=o, lse=lse)
+    assert device_error() == 0
+    return (o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64))
+
+
+def max_err(a, b):
+    if a.size == 0:
+        return 0.0
+    d = np.abs(a - b)
+    if np.isnan(d).any():
+        return float("inf")
+    return float(d.max())

@@ -1,0 +1,93 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared
+symbol, and rejects bad arguments before touching a device."""
+
+import os
+import re
+
+import pytest
+
+from exact_io_aware_107_b300 import _binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for must in ("attn_fwd", "attn_fwd_f32", "attn_strerror", "attn_get_device_error"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+        assert name in B._SIGNATURES, f"{name} has no ctypes signature"
+
+
+def test_version_and_strerror(lib):
+    assert B.attn_version() >= 100
+    for code in range(-9, 1):
+        s = B.strerror(code)
+        assert s and s != "unknown status"
+    assert B.strerror(-1234) == "unknown status"
+
+
+P = 1 << 20  # a 16-byte aligned stand-in address; never dereferenced on these paths
+
+
+@pytest.mark.parametrize("fn", [B.attn_fwd, B.attn_fwd_f32])
+def test_argument_errors_return_before_launch(lib, fn):
+    good = dict(q=P, k=P, v=P, o=P, lse=P, B=1, H=1, N=16, D=64, cu_seqlens=None, causal=1,
+                scale=0.125, stream=None)
+
+    def call(**kw):
+        a = dict(good, **kw)
+        return fn(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["D"],
+                  a["cu_seqlens"], a["causal"], a["scale"], a["stream"])
+
+    assert call(B=0) == B.ATTN_ERR_SHAPE
+    assert call(H=0) == B.ATTN_ERR_SHAPE
+    assert call(N=-1) == B.ATTN_ERR_SHAPE
+    assert call(scale=0.0) == B.ATTN_ERR_SCALE
+    assert call(scale=-1.0) == B.ATTN_ERR_SCALE
+    assert call(scale=float("inf")) == B.ATTN_ERR_SCALE
+    assert call(scale=float("nan")) == B.ATTN_ERR_SCALE
+    assert call(q=None) == B.ATTN_ERR_NULL
+    assert call(lse=None) == B.ATTN_ERR_NULL
+    assert call(o=P + 8) == B.ATTN_ERR_ALIGN
+    assert call(lse=P + 2) == B.ATTN_ERR_ALIGN
+    assert call(cu_seqlens=P + 1) == B.ATTN_ERR_ALIGN
+    assert call(D=0) == B.ATTN_ERR_HEADDIM
+    assert call(D=129) == B.ATTN_ERR_HEADDIM
+    # N == 0 is a no-op even with NULL pointers
+    assert call(N=0, q=None, k=None, v=None, o=None, lse=None) == B.ATTN_OK
+
+
+def test_bf16_head_dims(lib):
+    for d in (32, 96, 256):
+        assert B.attn_fwd(P, P, P, P, P, 1, 1, 16, d, None, 1, 0.1, None) == B.ATTN_ERR_HEADDIM
+
+
+def test_timeout_setter(lib):
+    assert B.attn_set_wait_timeout_ns(0) == B.ATTN_ERR_SHAPE
+    assert B.attn_set_wait_timeout_ns(10**9) == B.ATTN_OK
+    assert B.attn_wait_selftest(0, None) == B.ATTN_ERR_SHAPE
+
+
+def test_no_device_means_loud_failure(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    # valid arguments with no GPU: the call fails, it never computes on the CPU
+    assert B.attn_fwd(P, P, P, P, P, 1, 1, 16, 64, None, 1, 0.125, None) == B.ATTN_ERR_LAUNCH
+    assert B.attn_fwd_f32(P, P, P, P, P, 1, 1, 16, 64, None, 1, 0.125, None) == B.ATTN_ERR_LAUNCH
