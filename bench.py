@@ -68,61 +68,96 @@ def measured_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during a timed region."""
+    """SM clocks and throttle reasons sampled during a timed region.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NVML is polled every millisecond from a background thread (the timed
+    regions are tens of milliseconds long); if NVML is unavailable,
+    ``nvidia-smi -lms 10`` is used instead.
+    """
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.lines = []
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap"}
+
+    def __init__(self, local_index: int):
+        cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [t.strip() for t in cvd.split(",") if t.strip()]
+        self.gpu = int(ids[local_index]) if local_index < len(ids) and ids[local_index].isdigit() \
+            else local_index
+        self.samples = []       # (sm_mhz, max_mhz, reason_bits)
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
+        self.source = None
+
+    def _poll_nvml(self, nv, h):
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mx = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
+        while not self._stop.is_set():
+            try:
+                self.samples.append((nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM), mx,
+                                     int(get_reasons(h))))
+            except Exception:  # noqa: BLE001 - a failed query only loses one sample
+                pass
+            time.sleep(0.001)
+
+    def _read_smi(self):
+        for line in self._proc.stdout:
+            f = [x.strip() for x in line.split(",")]
+            try:
+                bits = 0
+                for bit, val in zip((0x8, 0x40, 0x20, 0x4), f[2:6]):
+                    bits |= bit if val.lower() == "active" else 0
+                self.samples.append((float(f[0]), float(f[1]), bits))
+            except (ValueError, IndexError):
+                continue
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self._t = threading.Thread(target=self._read, daemon=True)
-            self._t.start()
-        except (OSError, ValueError):
-            self.proc = None
+            import pynvml as nv
+            nv.nvmlInit()
+            h = nv.nvmlDeviceGetHandleByIndex(self.gpu)
+            self._thread = threading.Thread(target=self._poll_nvml, args=(nv, h), daemon=True)
+            self.source = "nvml"
+        except Exception:  # noqa: BLE001 - fall back to the command-line tool
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={self.gpu}",
+                     "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                     "clocks_event_reasons.hw_thermal_slowdown,"
+                     "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                     "--format=csv,noheader,nounits", "-lms", "10"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self._thread = threading.Thread(target=self._read_smi, daemon=True)
+                self.source = "nvidia-smi"
+                time.sleep(1.0)       # let the tool start before the timed region
+            except OSError:
+                self._thread = None
+        if self._thread is not None:
+            self._thread.start()
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
+                self._proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
         return False
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, val in zip(names, f[5:9]):
-                if val.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": self.source}
+        reasons = sorted({name for _, _, bits in self.samples
+                          for bit, name in self.REASONS.items() if bits & bit})
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_max_mhz": max(s[1] for s in self.samples), "reasons": reasons,
+                "samples": len(self.samples), "source": self.source}
 
 
 def dist_env():
@@ -160,6 +195,16 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
+def _blas_single_thread():
+    """One BLAS thread per worker thread, when threadpoolctl is available."""
+    try:
+        from threadpoolctl import threadpool_limits
+        return threadpool_limits(limits=1)
+    except ImportError:
+        import contextlib
+        return contextlib.nullcontext()
+
+
 def oracle_rows_sample(w, x, plane_index: int, rows: np.ndarray, threads: int):
     """Run the oracle on the given rows of one plane; returns (flops, seconds)."""
     import oracle
@@ -168,9 +213,8 @@ def oracle_rows_sample(w, x, plane_index: int, rows: np.ndarray, threads: int):
     q = W.as_f64(x["q"][b, h])
     k = W.as_f64(x["k"][b, h])
     v = W.as_f64(x["v"][b, h])
-    from threadpoolctl import threadpool_limits
     chunks = [c for c in np.array_split(rows, max(1, threads)) if len(c)]
-    with threadpool_limits(limits=1):
+    with _blas_single_thread():
         t0 = time.perf_counter()
         with ThreadPoolExecutor(max_workers=threads) as ex:
             list(ex.map(lambda r: oracle.attention_rows(q, k, v, w.scale, w.causal, r), chunks))
@@ -205,7 +249,7 @@ def run_reference(args, w):
         return 0
     x = W.generate(w)
     threads = host_cores()
-    rows = np.arange(w.N - 512, w.N)        # one step: 512 full-length rows of plane 0
+    rows = np.arange(max(0, w.N - 512), w.N)   # one step: the last 512 rows of plane 0
     for _ in range(args.warmup):
         oracle_rows_sample(w, x, 0, rows, threads)
     flops = secs = 0.0
@@ -221,7 +265,7 @@ def run_reference(args, w):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(w),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": f"each step: fp64 oracle on query rows {w.N - 512}..{w.N - 1} "
+                         "sample": f"each step: fp64 oracle on query rows {rows[0]}..{rows[-1]} "
                                    f"of plane (b=0,h=0) of {w.name}"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -336,6 +380,8 @@ def run_ours(args, w):
 
     peak_tf, _, peak_kind = load_peaks()
     achieved = flops / (kernel_ms * 1e-3) / 1e12
+    print(f"[bench] {w.name}: {ms_step:.3f} ms/step, {value:.1f} TFLOP/s, kernel {kernel_ms:.3f} ms"
+          f" ({achieved:.1f} TFLOP/s), e2e {e2e_ms:.3f} ms", file=sys.stderr)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -373,9 +419,16 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shape", default=None,
+                    help="B,H,N,D: same dtype and mask as --workload at another size "
+                         "(profiling cases)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     w = W.WORKLOADS[args.workload]
+    if args.shape:
+        b, h, n, d = (int(t) for t in args.shape.split(","))
+        w = W.custom(w.dtype, B=b, H=h, N=n, D=d, causal=w.causal, seed=w.seed, qk_std=w.qk_std,
+                     name=f"{w.dtype}_{'causal_' if w.causal else ''}b{b}_h{h}_n{n}_d{d}")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)
