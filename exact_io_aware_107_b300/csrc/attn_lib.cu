@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/attn_b300.h"
@@ -29,6 +30,7 @@ struct DeviceState {
   int checked = 0;  // 0 unknown, 1 ok, -1 wrong arch
   unsigned int* err = nullptr;
   bool attrs_set = false;
+  int sms = 0;
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -64,6 +66,11 @@ int prepare_device(DeviceState** out) {
         return ATTN_ERR_LAUNCH;
       }
       st.err = static_cast<unsigned int*>(p);
+      if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          st.sms < 1) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH;
+      }
       if (g_encode == nullptr) {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -179,14 +186,19 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   p.nseq = cu_seqlens ? B : 0;
   p.planes = planes;
   p.rows = N;
-  p.n_qblk = cu_seqlens ? (N / 256 + B) : (N + 255) / 256;
+  p.n_qblk = (N + 255) / 256;
+  // work items: packed -> single 256-row blocks (an upper bound, surplus
+  // entries are skipped); dense -> pairs of mirror blocks of one plane
+  const long long tiles = cu_seqlens ? (1LL * (N / 256 + B) * H) : (1LL * p.n_qblk * planes);
+  const long long items = cu_seqlens ? tiles : 1LL * ((p.n_qblk + 1) / 2) * planes;
+  if (tiles > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  p.n_tiles = static_cast<int>(tiles);
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns.load();
   p.err = st->err;
 
-  const long long grid = 1LL * p.n_qblk * planes;
-  if (grid > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  const long long grid = std::min<long long>(items, st->sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (D == 64)
     attn_fwd_bf16_kernel<64><<<static_cast<unsigned>(grid), Bf16Cfg<64>::THREADS,

@@ -1,5 +1,5 @@
-// bf16 attention forward for sm_103a: TMA + mbarrier pipeline, tcgen05 MMAs
-// with TMEM accumulators, online softmax in base 2.
+// bf16 attention forward for sm_103a: persistent CTAs, TMA + mbarrier
+// pipeline, tcgen05 MMAs with TMEM accumulators, online softmax in base 2.
 //
 // What it computes is the exact scaled-dot-product attention forward
 // O = softmax(scale * Q K^T + causal mask) V together with the per-row
@@ -14,13 +14,15 @@
 // Attention Mechanisms Explained", section "Causal Masking and Incremental
 // Decoding").
 //
-// CTA layout (320 threads, one CTA per SM):
+// CTA layout (320 threads, one persistent CTA per SM):
 //   warps 0-3  softmax for query tile 0 (thread t owns row t = TMEM lane t)
 //   warps 4-7  softmax for query tile 1
 //   warp  8    tcgen05 MMA issuer (lane 0) and TMEM owner
 //   warp  9    TMA producer (lane 0)
-// A CTA covers 256 query rows (two 128-row tiles) of one (batch, head) plane
-// or one packed sequence of one head.
+// A work tile is 256 query rows (two 128-row query tiles) of one (batch,
+// head) plane or of one packed sequence of one head.  Each CTA walks a
+// static list of work tiles (see bf16_tile); every role decodes the same
+// list, so they agree on the loop bounds without talking to each other.
 //
 // TMEM (512 columns x 128 lanes, fp32 cells):
 //   [  0,128) S0 = Q0 K^T   (P0 as packed bf16 overwrites its first 64 columns)
@@ -29,7 +31,8 @@
 //
 // Shared memory (1024-byte aligned; every tile is 128 rows x D bf16 stored as
 // D/64 chunks of 128 rows x 128 bytes, 128-byte swizzled, as TMA writes them):
-//   Q0, Q1, then NSTAGE ring slots holding K_0, V_0, K_1, V_1, ... in order.
+//   Q0, Q1, then NSTAGE ring slots holding K_0, V_0, K_1, V_1, ... of every
+//   work tile in turn.
 //
 // Rescaling is lazy: a row keeps its reference max until a tile raises the
 // max by more than 8 (base-2 units), so P stays <= 2^8 and most tiles need no
@@ -49,7 +52,8 @@ struct Bf16Params {
   int nseq;               // packed layout: number of sequences
   int planes;             // dense: B*H; packed: H
   int rows;               // dense: N; packed: total tokens
-  int n_qblk;             // dense: ceil(N/256); packed: upper bound on 256-row blocks
+  int n_qblk;             // dense: ceil(N/256)
+  int n_tiles;            // packed: an upper bound on the work tiles
   int causal;
   float scale_log2;       // scale * log2(e)
   unsigned long long timeout_ns;
@@ -60,15 +64,15 @@ template <int D>
 struct Bf16Cfg {
   static constexpr int BM = 128;                  // query rows per tile
   static constexpr int BN = 128;                  // keys per K/V tile
-  static constexpr int NSTAGE = (D == 128) ? 4 : 8;
+  static constexpr int NSTAGE = (D == 128) ? 5 : 10;
   static constexpr int CHUNK_BYTES = BM * 128;    // 128 rows x 128 bytes
   static constexpr int NCHUNK = D / 64;
   static constexpr int TILE_BYTES = BM * D * 2;
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = 2 * TILE_BYTES;
   static constexpr int BAR_OFF = KV_OFF + NSTAGE * TILE_BYTES;
-  // q_full, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], p_full[2], o_full[2], mma_done
-  static constexpr int NBAR = 1 + 2 * NSTAGE + 2 + 2 + 2 + 1;
+  // q_full, q_empty, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], p_full[2], o_full[2], mma_done
+  static constexpr int NBAR = 2 + 2 * NSTAGE + 2 + 2 + 2 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
@@ -80,36 +84,88 @@ struct Bf16Cfg {
   static_assert(SMEM_ALLOC <= 232448, "shared memory");
 };
 
-// Work decode, uniform across the CTA.  Returns false when the CTA has no work.
-__device__ __forceinline__ bool bf16_decode(const Bf16Params& p, int& plane, int& row_base,
-                                            int& seq_len, int& qblk) {
-  const int t = blockIdx.x;
-  plane = t % p.planes;
-  const int vb = t / p.planes;
+// One work tile: 256 query rows of one plane / sequence.
+struct WorkTile {
+  int plane;     // tensor-map plane coordinate (dense: b*H+h; packed: h)
+  int row_base;  // first row of the sequence in the tensor map (0 when dense)
+  int seq_len;   // keys (and query rows) of the sequence
+  int qblk;      // 256-row block index within the sequence
+  int n0, n1;    // key tiles visited by query tile 0 and 1 (0: tile absent)
+};
+
+// Cursor over packed sequences; every CTA's list positions increase, so the
+// walk over cu_seqlens only moves forward.
+struct SeqCursor {
+  int s = 0;
+  int cum = 0;  // 256-row blocks of the sequences before s
+};
+
+enum TileStep { kTileEnd = 0, kTileRun = 1, kTileSkip = 2 };
+
+// The it-th work tile of this CTA.
+//
+// Dense layout: the work list holds pairs of 256-row blocks of one plane,
+// block b with its mirror n-1-b, so that every pair costs the same under the
+// causal mask; pairs are plane-major (the CTAs in flight share few planes and
+// their K/V stay in L2).  Rounds of gridDim.x pairs go to the CTAs in
+// alternating direction; a CTA runs the heavy block of its pair, then the
+// light one (iteration it: pair round it/2, half it%2).
+//
+// Packed layout: the list holds single blocks, sequence by sequence, heaviest
+// block first, heads innermost; rounds alternate direction the same way.
+//
+// Returns kTileEnd past the last tile (or when cu_seqlens is malformed),
+// kTileSkip for the empty second half of a pair whose two blocks coincide.
+__device__ __forceinline__ int bf16_tile(const Bf16Params& p, int it, SeqCursor& cur,
+                                         WorkTile& w) {
+  const int grid = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
   if (p.cu_seqlens == nullptr) {
-    // heaviest causal blocks (largest query index) are launched first
-    qblk = p.n_qblk - 1 - vb;
-    row_base = 0;
-    seq_len = p.rows;
-    return qblk >= 0;
-  }
-  int cum = 0;
-  for (int s = 0; s < p.nseq; ++s) {
-    const int a = __ldg(p.cu_seqlens + s), e = __ldg(p.cu_seqlens + s + 1);
-    if (a < 0 || e < a || e > p.rows) {
-      if (threadIdx.x == 0) atomicOr(p.err, kDevErrBounds);
-      return false;
+    const int round = it >> 1;
+    const int pair = round * grid + ((round & 1) ? grid - 1 - c : c);
+    const int npp = (p.n_qblk + 1) / 2;  // pairs per plane
+    if (pair >= p.planes * npp) return kTileEnd;
+    w.plane = pair / npp;
+    const int pb = pair - w.plane * npp;
+    const int heavy = p.n_qblk - 1 - pb;
+    if (it & 1) {
+      if (pb == heavy) return kTileSkip;
+      w.qblk = pb;
+    } else {
+      w.qblk = heavy;
     }
-    const int nb = (e - a + 255) / 256;
-    if (vb < cum + nb) {
-      row_base = a;
-      seq_len = e - a;
-      qblk = nb - 1 - (vb - cum);
-      return true;
+    w.row_base = 0;
+    w.seq_len = p.rows;
+  } else {
+    const int u = it * grid + ((it & 1) ? grid - 1 - c : c);
+    if (u >= p.n_tiles) return kTileEnd;
+    const int vb = u / p.planes;
+    w.plane = u - vb * p.planes;
+    bool found = false;
+    while (cur.s < p.nseq) {
+      const int a = __ldg(p.cu_seqlens + cur.s), e = __ldg(p.cu_seqlens + cur.s + 1);
+      if (a < 0 || e < a || e > p.rows) {
+        if (threadIdx.x == 0) atomicOr(p.err, kDevErrBounds);
+        return kTileEnd;
+      }
+      const int nb = (e - a + 255) / 256;
+      if (vb < cur.cum + nb) {
+        w.row_base = a;
+        w.seq_len = e - a;
+        w.qblk = nb - 1 - (vb - cur.cum);
+        found = true;
+        break;
+      }
+      cur.cum += nb;
+      ++cur.s;
     }
-    cum += nb;
+    if (!found) return kTileEnd;
   }
-  return false;
+  const int nkv = (w.seq_len + 127) / 128;
+  const bool has_q1 = w.qblk * 256 + 128 < w.seq_len;
+  w.n0 = p.causal ? min(nkv, 2 * w.qblk + 1) : nkv;
+  w.n1 = has_q1 ? (p.causal ? min(nkv, 2 * w.qblk + 2) : nkv) : 0;
+  return kTileRun;
 }
 
 template <int D>
@@ -150,7 +206,8 @@ __global__ void __launch_bounds__(320, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* kv_full = bars + 2;
   uint64_t* kv_empty = kv_full + NS;
   uint64_t* s_full = kv_empty + NS;
   uint64_t* p_full = s_full + 2;
@@ -159,14 +216,18 @@ __global__ void __launch_bounds__(320, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
-  int plane, row_base, seq_len, qblk;
-  if (!bf16_decode(p, plane, row_base, seq_len, qblk)) return;
+  {
+    SeqCursor c0;
+    WorkTile w0;
+    if (bf16_tile(p, 0, c0, w0) != kTileRun) return;  // uniform: no work for this CTA
+  }
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
@@ -189,98 +250,113 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
-
-  const int q_row0 = qblk * 256;  // first query row of the CTA, relative to the sequence
-  const bool has_q1 = q_row0 + 128 < seq_len;
-  const int nkv = (seq_len + C::BN - 1) / C::BN;
-  const int n0 = p.causal ? min(nkv, 2 * qblk + 1) : nkv;
-  const int n1 = has_q1 ? (p.causal ? min(nkv, 2 * qblk + 2) : nkv) : 0;
-  const int nmax = max(n0, n1);
   const uint32_t smem_base = smem_u32(smem);
 
   if (warp < 8) {
     // ------------------------------------------------------------ softmax
-    const int ti = warp / 4;              // query tile
+    const int ti = warp / 4;               // query tile of this warpgroup
     const int t = threadIdx.x - 128 * ti;  // row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
     const uint32_t tS = tmem + lane_off + (ti ? C::S_COL1 : C::S_COL0);
     const uint32_t tO = tmem + lane_off + (ti ? C::O_COL1 : C::O_COL0);
-    const int n_i = ti ? n1 : n0;
-    const int row = q_row0 + 128 * ti + t;
     const float cl2 = p.scale_log2;
-    float m_ref = -INFINITY;
-    float l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_i; ++j) {
-      if (!mbar_wait(&s_full[ti], j & 1, ctl)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[128];
-      tmem_ld64_wait(tS, *reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
-      tmem_ld64_wait(tS + 64, *reinterpret_cast<uint32_t(*)[64]>(&sr[64]));
-      float* s = reinterpret_cast<float*>(sr);
-      const int kv0 = j * C::BN;
-      const bool need_mask = (kv0 + C::BN > seq_len) || (p.causal && kv0 + C::BN - 1 > q_row0 + 128 * ti);
-      if (need_mask) {
-        const int lim = p.causal ? min(seq_len - 1, row) : (seq_len - 1);
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (kv0 + c > lim) s[c] = -INFINITY;
-      }
-      float mx[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = s[e];
-#pragma unroll
-      for (int c = 8; c < 128; c += 8)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], s[c + e]);
-      const float mt =
-          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cl2;
-      float m_new = m_ref;
-      float alpha = 1.f;
-      bool resc = false;
-      if (mt > m_ref + 8.f) {
-        m_new = mt;
-        alpha = ex2_approx(m_ref - m_new);
-        resc = (j > 0);
-      }
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      float sum[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float a = ex2_approx(fmaf(s[2 * c], cl2, -m_use));
-        const float b = ex2_approx(fmaf(s[2 * c + 1], cl2, -m_use));
-        sum[(2 * c) & 3] += a;
-        sum[(2 * c + 1) & 3] += b;
-        pk[c] = pack_bf16x2(a, b);
-      }
-      l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
-      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-      if (__any_sync(0xffffffffu, resc)) {
-        const float f = resc ? alpha : 1.f;
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32_wait(tO + 32 * cc, o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-          tmem_st32(tO + 32 * cc, o);
+    const uint64_t c2 = f32x2(cl2, cl2);
+    uint32_t n_s = 0, n_o = 0;  // s_full / o_full phases consumed so far
+    SeqCursor cur;
+    WorkTile w;
+    for (int it = 0;; ++it) {
+      const int step = bf16_tile(p, it, cur, w);
+      if (step == kTileEnd) break;
+      const int n_i = ti ? w.n1 : w.n0;
+      if (step == kTileSkip || n_i == 0) continue;
+      const int q_first = w.qblk * 256 + 128 * ti;  // first row of this query tile
+      const int row = q_first + t;
+      float m_ref = -INFINITY;
+      float l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < n_i; ++j) {
+        // warp-uniform outcome: the TMEM loads below are warp-collective
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[ti], n_s & 1, ctl))) {
+          ok = false;
+          break;
         }
+        ++n_s;
+        tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld128_wait(tS, sr);
+        const int kv0 = j * C::BN;
+        const bool need_mask =
+            (kv0 + C::BN > w.seq_len) || (p.causal && kv0 + C::BN - 1 > q_first);
+        if (need_mask) {
+          const int lim = p.causal ? min(w.seq_len - 1, row) : (w.seq_len - 1);
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (kv0 + c > lim) sr[c] = __float_as_uint(-INFINITY);
+        }
+        // row max: four independent chains of three-input maxima
+        float mx[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          mx[e] = fmax3(__uint_as_float(sr[e]), __uint_as_float(sr[e + 4]),
+                        __uint_as_float(sr[e + 8]));
+#pragma unroll
+        for (int c = 12; c < 124; c += 8)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            mx[e] = fmax3(mx[e], __uint_as_float(sr[c + e]), __uint_as_float(sr[c + 4 + e]));
+        const float tail = fmax3(__uint_as_float(sr[124]), __uint_as_float(sr[125]),
+                                 fmaxf(__uint_as_float(sr[126]), __uint_as_float(sr[127])));
+        const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], tail) * cl2;
+        float m_new = m_ref;
+        float alpha = 1.f;
+        bool resc = false;
+        if (mt > m_ref + 8.f) {
+          m_new = mt;
+          alpha = ex2_approx(m_ref - m_new);
+          resc = (j > 0);
+        }
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const uint64_t nm2 = f32x2(-m_use, -m_use);
+        uint64_t acc2[2] = {0ull, 0ull};
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const uint64_t x2 = ffma2(u32x2(sr[2 * c], sr[2 * c + 1]), c2, nm2);
+          const float a = ex2_approx(lo_f32(x2));
+          const float b = ex2_approx(hi_f32(x2));
+          acc2[c & 1] = fadd2(acc2[c & 1], f32x2(a, b));
+          pk[c] = pack_bf16x2(a, b);
+        }
+        const uint64_t sum2 = fadd2(acc2[0], acc2[1]);
+        l = l * alpha + (lo_f32(sum2) + hi_f32(sum2));
+        tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        if (__any_sync(0xffffffffu, resc)) {
+          const float f = resc ? alpha : 1.f;
+          const uint64_t f2 = f32x2(f, f);
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32_wait(tO + 32 * cc, o);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const uint64_t v = fmul2(u32x2(o[2 * e], o[2 * e + 1]), f2);
+              o[2 * e] = static_cast<uint32_t>(v);
+              o[2 * e + 1] = static_cast<uint32_t>(v >> 32);
+            }
+            tmem_st32(tO + 32 * cc, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&p_full[ti]);
+        m_ref = m_new;
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&p_full[ti]);
-      m_ref = m_new;
-    }
-    if (ok && n_i > 0 && mbar_wait(&o_full[ti], 0, ctl)) {
+      if (!ok || !__all_sync(0xffffffffu, mbar_wait(&o_full[ti], n_o & 1, ctl))) break;
+      ++n_o;
       tc_fence_after();
-      const bool valid = row < seq_len;
-      const size_t grow = static_cast<size_t>(plane) * p.rows + row_base + row;
+      const bool valid = row < w.seq_len;
+      const size_t grow = static_cast<size_t>(w.plane) * p.rows + w.row_base + row;
       const float inv_l = 1.f / l;
       uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D);
 #pragma unroll
@@ -290,7 +366,8 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t h[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          h[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+          h[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
+                             __uint_as_float(o[2 * e + 1]) * inv_l);
         if (valid) {
 #pragma unroll
           for (int v = 0; v < 4; ++v)
@@ -305,48 +382,72 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t q0 = smem_base + C::Q_OFF;
       const uint32_t q1 = q0 + C::TILE_BYTES;
       const uint32_t kvb = smem_base + C::KV_OFF;
-      bool ok = mbar_wait(q_full, 0, ctl);
-      if (ok) ok = mbar_wait(&kv_full[0], 0, ctl);
-      if (ok) {
+      uint32_t n_q = 0, n_p[2] = {0, 0};
+      int g = 0;  // ring position of the tile's K_0
+      bool ok = true;
+      SeqCursor cur;
+      WorkTile w;
+      for (int it = 0; ok; ++it) {
+        const int step = bf16_tile(p, it, cur, w);
+        if (step == kTileEnd) break;
+        if (step == kTileSkip) continue;
+        const int nmax = max(w.n0, w.n1);
+        int s_left = w.n0 + w.n1;  // S groups still to issue; Q is free after the last
+        if (!mbar_wait(q_full, n_q & 1, ctl) ||
+            !mbar_wait(&kv_full[g % NS], (g / NS) & 1, ctl)) {
+          ok = false;
+          break;
+        }
+        ++n_q;
         tc_fence_after();
-        if (n0 > 0) {
-          bf16_issue_s<D>(tmem + C::S_COL0, q0, kvb);
+        const uint32_t k0 = kvb + (g % NS) * C::TILE_BYTES;
+        if (w.n0 > 0) {
+          bf16_issue_s<D>(tmem + C::S_COL0, q0, k0);
           umma_commit(&s_full[0]);
+          --s_left;
         }
-        if (n1 > 0) {
-          bf16_issue_s<D>(tmem + C::S_COL1, q1, kvb);
+        if (w.n1 > 0) {
+          bf16_issue_s<D>(tmem + C::S_COL1, q1, k0);
           umma_commit(&s_full[1]);
+          --s_left;
         }
-        umma_commit(&kv_empty[0]);
-      }
-      for (int j = 0; ok && j < nmax; ++j) {
-        const int tv = 2 * j + 1, tk = 2 * j + 2;
-        const int sv = tv % NS, sk = tk % NS;
-        const bool next = j + 1 < nmax;
-        if (!mbar_wait(&kv_full[sv], (tv / NS) & 1, ctl)) break;
-        if (next && !mbar_wait(&kv_full[sk], (tk / NS) & 1, ctl)) break;
-        tc_fence_after();
-        for (int ti = 0; ti < 2; ++ti) {
-          const int n_i = ti ? n1 : n0;
-          if (j >= n_i) continue;
-          if (!mbar_wait(&p_full[ti], j & 1, ctl)) {
+        if (s_left == 0) umma_commit(q_empty);
+        umma_commit(&kv_empty[g % NS]);
+        for (int j = 0; j < nmax; ++j) {
+          const int gv = g + 2 * j + 1, gk = g + 2 * j + 2;
+          const bool next = j + 1 < nmax;
+          if (!mbar_wait(&kv_full[gv % NS], (gv / NS) & 1, ctl) ||
+              (next && !mbar_wait(&kv_full[gk % NS], (gk / NS) & 1, ctl))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sc = ti ? C::S_COL1 : C::S_COL0;
-          const uint32_t oc = ti ? C::O_COL1 : C::O_COL0;
-          bf16_issue_pv<D>(tmem + oc, tmem + sc, kvb + sv * C::TILE_BYTES, j > 0 ? 1u : 0u);
-          if (j + 1 < n_i) {
-            bf16_issue_s<D>(tmem + sc, ti ? q1 : q0, kvb + sk * C::TILE_BYTES);
-            umma_commit(&s_full[ti]);
-          } else {
-            umma_commit(&o_full[ti]);
+          for (int ti = 0; ti < 2; ++ti) {
+            const int n_i = ti ? w.n1 : w.n0;
+            if (j >= n_i) continue;
+            if (!mbar_wait(&p_full[ti], n_p[ti] & 1, ctl)) {
+              ok = false;
+              break;
+            }
+            ++n_p[ti];
+            tc_fence_after();
+            const uint32_t sc = ti ? C::S_COL1 : C::S_COL0;
+            const uint32_t oc = ti ? C::O_COL1 : C::O_COL0;
+            bf16_issue_pv<D>(tmem + oc, tmem + sc, kvb + (gv % NS) * C::TILE_BYTES,
+                             j > 0 ? 1u : 0u);
+            if (j + 1 < n_i) {
+              bf16_issue_s<D>(tmem + sc, ti ? q1 : q0, kvb + (gk % NS) * C::TILE_BYTES);
+              umma_commit(&s_full[ti]);
+              if (--s_left == 0) umma_commit(q_empty);
+            } else {
+              umma_commit(&o_full[ti]);
+            }
           }
+          if (!ok) break;
+          umma_commit(&kv_empty[gv % NS]);
+          if (next) umma_commit(&kv_empty[gk % NS]);
         }
-        if (!ok) break;
-        umma_commit(&kv_empty[sv]);
-        if (next) umma_commit(&kv_empty[sk]);
+        g += 2 * nmax;
       }
       // every MMA issued so far must finish before TMEM and shared memory are released
       umma_commit(mma_done);
@@ -358,34 +459,46 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      const int pc = plane;
-      const int qr = row_base + q_row0;
-      mbar_arrive_expect_tx(q_full, (has_q1 ? 2 : 1) * C::TILE_BYTES);
-#pragma unroll
-      for (int c = 0; c < C::NCHUNK; ++c)
-        tma_load_3d(smem + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, qr, pc);
-      if (has_q1) {
-#pragma unroll
-        for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(smem + C::Q_OFF + C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64,
-                      qr + 128, pc);
-      }
-      int issued = 0;
-      for (int t = 0; t < 2 * nmax; ++t) {
-        const int s = t % NS, u = t / NS;
-        if (u > 0 && !mbar_wait(&kv_empty[s], (u - 1) & 1, ctl)) break;
-        const int j = t >> 1;
-        const CUtensorMap* m = (t & 1) ? &tmV : &tmK;
-        mbar_arrive_expect_tx(&kv_full[s], C::TILE_BYTES);
+      uint32_t n_q = 0;
+      int g = 0;  // ring positions issued
+      bool ok = true;
+      SeqCursor cur;
+      WorkTile w;
+      for (int it = 0; ok; ++it) {
+        const int step = bf16_tile(p, it, cur, w);
+        if (step == kTileEnd) break;
+        if (step == kTileSkip) continue;
+        const int nmax = max(w.n0, w.n1);
+        if (n_q > 0 && !mbar_wait(q_empty, (n_q - 1) & 1, ctl)) break;
+        const int qr = w.row_base + w.qblk * 256;
+        mbar_arrive_expect_tx(q_full, (w.n1 > 0 ? 2 : 1) * C::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(smem + C::KV_OFF + s * C::TILE_BYTES + c * C::CHUNK_BYTES, m, &kv_full[s],
-                      c * 64, row_base + j * C::BN, pc);
-        issued = t + 1;
+          tma_load_3d(smem + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, qr, w.plane);
+        if (w.n1 > 0) {
+#pragma unroll
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_3d(smem + C::Q_OFF + C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ, q_full,
+                        c * 64, qr + 128, w.plane);
+        }
+        ++n_q;
+        for (int t = 0; t < 2 * nmax; ++t, ++g) {
+          const int s = g % NS, u = g / NS;
+          if (u > 0 && !mbar_wait(&kv_empty[s], (u - 1) & 1, ctl)) {
+            ok = false;
+            break;
+          }
+          const CUtensorMap* m = (t & 1) ? &tmV : &tmK;
+          mbar_arrive_expect_tx(&kv_full[s], C::TILE_BYTES);
+#pragma unroll
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_3d(smem + C::KV_OFF + s * C::TILE_BYTES + c * C::CHUNK_BYTES, m,
+                        &kv_full[s], c * 64, w.row_base + (t >> 1) * C::BN, w.plane);
+        }
       }
       // drain: every copy issued must land before the CTA may exit
-      mbar_wait_drain(q_full, 0, ctl);
-      for (int t = max(0, issued - NS); t < issued; ++t)
+      if (n_q > 0) mbar_wait_drain(q_full, (n_q - 1) & 1, ctl);
+      for (int t = max(0, g - NS); t < g; ++t)
         mbar_wait_drain(&kv_full[t % NS], (t / NS) & 1, ctl);
     }
   }
