@@ -15,8 +15,9 @@
 // Decoding").
 //
 // CTA layout (320 threads, one persistent CTA per SM):
-//   warps 0-3  softmax for query tile 0 (thread t owns row t = TMEM lane t)
-//   warps 4-7  softmax for query tile 1
+//   warps 0-3  softmax and epilogue for query tile 0 (thread t owns row t =
+//              TMEM lane t)
+//   warps 4-7  softmax and epilogue for query tile 1
 //   warp  8    tcgen05 MMA issuer (lane 0) and TMEM owner
 //   warp  9    TMA producer (lane 0)
 // A work tile is 256 query rows (two 128-row query tiles) of one (batch,
@@ -31,8 +32,11 @@
 //
 // Shared memory (1024-byte aligned; every tile is 128 rows x D bf16 stored as
 // D/64 chunks of 128 rows x 128 bytes, 128-byte swizzled, as TMA writes them):
-//   Q0, Q1, then NSTAGE ring slots holding K_0, V_0, K_1, V_1, ... of every
-//   work tile in turn.
+//   Q0, Q1 (each with its own full/empty barriers, so the next work tile's
+//   Q0 loads as soon as the last S0 of the current one is done), then NSTAGE
+//   ring slots holding K_0, V_0, K_1, V_1, ... of every work tile in turn.
+//   The producer issues the next tile's K_0 and V_0 before it waits for the
+//   Q buffers, so a tile change costs little more than one Q load.
 //
 // Rescaling is lazy: a row keeps its reference max until a tile raises the
 // max by more than 8 (base-2 units), so P stays <= 2^8 and most tiles need no
@@ -71,8 +75,9 @@ struct Bf16Cfg {
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = 2 * TILE_BYTES;
   static constexpr int BAR_OFF = KV_OFF + NSTAGE * TILE_BYTES;
-  // q_full, q_empty, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], p_full[2], o_full[2], mma_done
-  static constexpr int NBAR = 2 + 2 * NSTAGE + 2 + 2 + 2 + 1;
+  // q_full[2], q_empty[2], kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], p_full[2],
+  // o_full[2], mma_done
+  static constexpr int NBAR = 4 + 2 * NSTAGE + 6 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
@@ -205,13 +210,13 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  uint64_t* q_full = bars;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* kv_full = bars + 2;
+  uint64_t* q_full = bars;          // [2]
+  uint64_t* q_empty = bars + 2;     // [2]
+  uint64_t* kv_full = bars + 4;     // [NS]
   uint64_t* kv_empty = kv_full + NS;
-  uint64_t* s_full = kv_empty + NS;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_full = p_full + 2;
+  uint64_t* s_full = kv_empty + NS;  // [2]
+  uint64_t* p_full = s_full + 2;     // [2]
+  uint64_t* o_full = p_full + 2;     // [2]
   uint64_t* mma_done = o_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
@@ -226,16 +231,16 @@ __global__ void __launch_bounds__(320, 1)
   const int lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
-    }
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&o_full[i], 1);
+    }
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -379,10 +384,9 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t q0 = smem_base + C::Q_OFF;
-      const uint32_t q1 = q0 + C::TILE_BYTES;
+      const uint32_t qb[2] = {smem_base + C::Q_OFF, smem_base + C::Q_OFF + C::TILE_BYTES};
       const uint32_t kvb = smem_base + C::KV_OFF;
-      uint32_t n_q = 0, n_p[2] = {0, 0};
+      uint32_t n_q[2] = {0, 0}, n_p[2] = {0, 0};
       int g = 0;  // ring position of the tile's K_0
       bool ok = true;
       SeqCursor cur;
@@ -392,26 +396,25 @@ __global__ void __launch_bounds__(320, 1)
         if (step == kTileEnd) break;
         if (step == kTileSkip) continue;
         const int nmax = max(w.n0, w.n1);
-        int s_left = w.n0 + w.n1;  // S groups still to issue; Q is free after the last
-        if (!mbar_wait(q_full, n_q & 1, ctl) ||
-            !mbar_wait(&kv_full[g % NS], (g / NS) & 1, ctl)) {
+        if (!mbar_wait(&kv_full[g % NS], (g / NS) & 1, ctl)) {
           ok = false;
           break;
         }
-        ++n_q;
-        tc_fence_after();
         const uint32_t k0 = kvb + (g % NS) * C::TILE_BYTES;
-        if (w.n0 > 0) {
-          bf16_issue_s<D>(tmem + C::S_COL0, q0, k0);
-          umma_commit(&s_full[0]);
-          --s_left;
+        for (int ti = 0; ti < 2; ++ti) {
+          const int n_i = ti ? w.n1 : w.n0;
+          if (n_i == 0) continue;
+          if (!mbar_wait(&q_full[ti], n_q[ti] & 1, ctl)) {
+            ok = false;
+            break;
+          }
+          ++n_q[ti];
+          tc_fence_after();
+          bf16_issue_s<D>(tmem + (ti ? C::S_COL1 : C::S_COL0), qb[ti], k0);
+          umma_commit(&s_full[ti]);
+          if (n_i == 1) umma_commit(&q_empty[ti]);
         }
-        if (w.n1 > 0) {
-          bf16_issue_s<D>(tmem + C::S_COL1, q1, k0);
-          umma_commit(&s_full[1]);
-          --s_left;
-        }
-        if (s_left == 0) umma_commit(q_empty);
+        if (!ok) break;
         umma_commit(&kv_empty[g % NS]);
         for (int j = 0; j < nmax; ++j) {
           const int gv = g + 2 * j + 1, gk = g + 2 * j + 2;
@@ -436,9 +439,9 @@ __global__ void __launch_bounds__(320, 1)
             bf16_issue_pv<D>(tmem + oc, tmem + sc, kvb + (gv % NS) * C::TILE_BYTES,
                              j > 0 ? 1u : 0u);
             if (j + 1 < n_i) {
-              bf16_issue_s<D>(tmem + sc, ti ? q1 : q0, kvb + (gk % NS) * C::TILE_BYTES);
+              bf16_issue_s<D>(tmem + sc, qb[ti], kvb + (gk % NS) * C::TILE_BYTES);
               umma_commit(&s_full[ti]);
-              if (--s_left == 0) umma_commit(q_empty);
+              if (j + 2 == n_i) umma_commit(&q_empty[ti]);  // that was the last S of Q_ti
             } else {
               umma_commit(&o_full[ti]);
             }
@@ -459,45 +462,50 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      uint32_t n_q = 0;
+      uint32_t n_q[2] = {0, 0};
       int g = 0;  // ring positions issued
       bool ok = true;
       SeqCursor cur;
       WorkTile w;
+      // one K or V tile into the next ring slot
+      auto load_kv = [&](int t) -> bool {
+        const int s = g % NS, u = g / NS;
+        if (u > 0 && !mbar_wait(&kv_empty[s], (u - 1) & 1, ctl)) return false;
+        mbar_arrive_expect_tx(&kv_full[s], C::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(smem + C::KV_OFF + s * C::TILE_BYTES + c * C::CHUNK_BYTES,
+                      (t & 1) ? &tmV : &tmK, &kv_full[s], c * 64, w.row_base + (t >> 1) * C::BN,
+                      w.plane);
+        ++g;
+        return true;
+      };
       for (int it = 0; ok; ++it) {
         const int step = bf16_tile(p, it, cur, w);
         if (step == kTileEnd) break;
         if (step == kTileSkip) continue;
-        const int nmax = max(w.n0, w.n1);
-        if (n_q > 0 && !mbar_wait(q_empty, (n_q - 1) & 1, ctl)) break;
-        const int qr = w.row_base + w.qblk * 256;
-        mbar_arrive_expect_tx(q_full, (w.n1 > 0 ? 2 : 1) * C::TILE_BYTES);
-#pragma unroll
-        for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(smem + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, qr, w.plane);
-        if (w.n1 > 0) {
-#pragma unroll
-          for (int c = 0; c < C::NCHUNK; ++c)
-            tma_load_3d(smem + C::Q_OFF + C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ, q_full,
-                        c * 64, qr + 128, w.plane);
-        }
-        ++n_q;
-        for (int t = 0; t < 2 * nmax; ++t, ++g) {
-          const int s = g % NS, u = g / NS;
-          if (u > 0 && !mbar_wait(&kv_empty[s], (u - 1) & 1, ctl)) {
+        const int nkv = 2 * max(w.n0, w.n1);
+        // K_0 and V_0 first: their slots are freed by the previous tile alone
+        const int head = min(2, nkv);
+        for (int t = 0; ok && t < head; ++t) ok = load_kv(t);
+        for (int ti = 0; ok && ti < 2; ++ti) {
+          if ((ti ? w.n1 : w.n0) == 0) continue;
+          if (n_q[ti] > 0 && !mbar_wait(&q_empty[ti], (n_q[ti] - 1) & 1, ctl)) {
             ok = false;
             break;
           }
-          const CUtensorMap* m = (t & 1) ? &tmV : &tmK;
-          mbar_arrive_expect_tx(&kv_full[s], C::TILE_BYTES);
+          mbar_arrive_expect_tx(&q_full[ti], C::TILE_BYTES);
 #pragma unroll
           for (int c = 0; c < C::NCHUNK; ++c)
-            tma_load_3d(smem + C::KV_OFF + s * C::TILE_BYTES + c * C::CHUNK_BYTES, m,
-                        &kv_full[s], c * 64, w.row_base + (t >> 1) * C::BN, w.plane);
+            tma_load_3d(smem + C::Q_OFF + ti * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ,
+                        &q_full[ti], c * 64, w.row_base + w.qblk * 256 + 128 * ti, w.plane);
+          ++n_q[ti];
         }
+        for (int t = head; ok && t < nkv; ++t) ok = load_kv(t);
       }
       // drain: every copy issued must land before the CTA may exit
-      if (n_q > 0) mbar_wait_drain(q_full, (n_q - 1) & 1, ctl);
+      for (int ti = 0; ti < 2; ++ti)
+        if (n_q[ti] > 0) mbar_wait_drain(&q_full[ti], (n_q[ti] - 1) & 1, ctl);
       for (int t = max(0, g - NS); t < g; ++t)
         mbar_wait_drain(&kv_full[t % NS], (t / NS) & 1, ctl);
     }
