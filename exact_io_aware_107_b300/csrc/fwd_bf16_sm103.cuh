@@ -173,29 +173,32 @@ __device__ __forceinline__ int bf16_tile(const Bf16Params& p, int it, SeqCursor&
   return kTileRun;
 }
 
+// S = Q K^T for one 128x128 tile: D/16 MMAs of K=16.  q_desc/k_desc are the
+// descriptors of the tiles' first bytes; the start-address field (bits 0-13,
+// bytes / 16) is advanced in place, which cannot carry out of the field
+// because shared addresses stay below 256 KB.
 template <int D>
-__device__ __forceinline__ void bf16_issue_s(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void bf16_issue_s(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
   using C = Bf16Cfg<D>;
   constexpr uint32_t idesc = idesc_bf16_f32(128, C::BN, 0, 0);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32;
-    const uint64_t a = sdesc_sw128(q_smem + off, 16, 1024);
-    const uint64_t b = sdesc_sw128(k_smem + off, 16, 1024);
-    umma_ss(d_tmem, a, b, idesc, kk > 0 ? 1u : 0u);
+    const uint32_t off = ((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
+    umma_ss_warp(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
+// O (+)= P V: P (bf16 pairs) from TMEM columns p_tmem.., V tile from v_desc.
 template <int D>
-__device__ __forceinline__ void bf16_issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+__device__ __forceinline__ void bf16_issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                               uint32_t accumulate) {
   using C = Bf16Cfg<D>;
   constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
 #pragma unroll
   for (int kk = 0; kk < C::BN / 16; ++kk) {
     // V is the MN-major B operand: 16 keys = two 8-row groups of 128-byte rows
-    const uint64_t b = sdesc_sw128(v_smem + kk * 16 * 128, C::CHUNK_BYTES, 1024);
-    umma_ts(d_tmem, p_tmem + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    umma_ts_warp(d_tmem, p_tmem + kk * 8, v_desc + ((kk * 16 * 128) >> 4), idesc,
+                 (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -383,132 +386,143 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t qb[2] = {smem_base + C::Q_OFF, smem_base + C::Q_OFF + C::TILE_BYTES};
-      const uint32_t kvb = smem_base + C::KV_OFF;
-      uint32_t n_q[2] = {0, 0}, n_p[2] = {0, 0};
-      int g = 0;  // ring position of the tile's K_0
-      bool ok = true;
-      SeqCursor cur;
-      WorkTile w;
-      for (int it = 0; ok; ++it) {
-        const int step = bf16_tile(p, it, cur, w);
-        if (step == kTileEnd) break;
-        if (step == kTileSkip) continue;
-        const int nmax = max(w.n0, w.n1);
-        if (!mbar_wait(&kv_full[g % NS], (g / NS) & 1, ctl)) {
+    // The whole warp runs this loop so every operand is warp-uniform; one
+    // elected lane issues each tcgen05 instruction.
+    const uint64_t qd[2] = {sdesc_sw128(smem_base + C::Q_OFF, 16, 1024),
+                            sdesc_sw128(smem_base + C::Q_OFF + C::TILE_BYTES, 16, 1024)};
+    const uint64_t kd0 = sdesc_sw128(smem_base + C::KV_OFF, 16, 1024);
+    const uint64_t vd0 = sdesc_sw128(smem_base + C::KV_OFF, C::CHUNK_BYTES, 1024);
+    constexpr uint32_t kSlotDesc = C::TILE_BYTES >> 4;  // descriptor step between ring slots
+    uint32_t n_q[2] = {0, 0}, n_p[2] = {0, 0};
+    int g = 0;  // ring position of the tile's K_0
+    bool ok = true;
+    SeqCursor cur;
+    WorkTile w;
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl));
+    };
+    for (int it = 0; ok; ++it) {
+      const int step = bf16_tile(p, it, cur, w);
+      if (step == kTileEnd) break;
+      if (step == kTileSkip) continue;
+      const int nmax = max(w.n0, w.n1);
+      if (!wait(&kv_full[g % NS], (g / NS) & 1)) {
+        ok = false;
+        break;
+      }
+      const uint64_t k0 = kd0 + (g % NS) * kSlotDesc;
+      for (int ti = 0; ti < 2; ++ti) {
+        const int n_i = ti ? w.n1 : w.n0;
+        if (n_i == 0) continue;
+        if (!wait(&q_full[ti], n_q[ti] & 1)) {
           ok = false;
           break;
         }
-        const uint32_t k0 = kvb + (g % NS) * C::TILE_BYTES;
+        ++n_q[ti];
+        tc_fence_after();
+        bf16_issue_s<D>(tmem + (ti ? C::S_COL1 : C::S_COL0), qd[ti], k0);
+        umma_commit_warp(&s_full[ti]);
+        if (n_i == 1) umma_commit_warp(&q_empty[ti]);
+      }
+      if (!ok) break;
+      umma_commit_warp(&kv_empty[g % NS]);
+      for (int j = 0; j < nmax; ++j) {
+        const int gv = g + 2 * j + 1, gk = g + 2 * j + 2;
+        const bool next = j + 1 < nmax;
+        if (!wait(&kv_full[gv % NS], (gv / NS) & 1) ||
+            (next && !wait(&kv_full[gk % NS], (gk / NS) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         for (int ti = 0; ti < 2; ++ti) {
           const int n_i = ti ? w.n1 : w.n0;
-          if (n_i == 0) continue;
-          if (!mbar_wait(&q_full[ti], n_q[ti] & 1, ctl)) {
+          if (j >= n_i) continue;
+          if (!wait(&p_full[ti], n_p[ti] & 1)) {
             ok = false;
             break;
           }
-          ++n_q[ti];
+          ++n_p[ti];
           tc_fence_after();
-          bf16_issue_s<D>(tmem + (ti ? C::S_COL1 : C::S_COL0), qb[ti], k0);
-          umma_commit(&s_full[ti]);
-          if (n_i == 1) umma_commit(&q_empty[ti]);
+          const uint32_t sc = ti ? C::S_COL1 : C::S_COL0;
+          const uint32_t oc = ti ? C::O_COL1 : C::O_COL0;
+          bf16_issue_pv<D>(tmem + oc, tmem + sc, vd0 + (gv % NS) * kSlotDesc, j > 0 ? 1u : 0u);
+          if (j + 1 < n_i) {
+            bf16_issue_s<D>(tmem + sc, qd[ti], kd0 + (gk % NS) * kSlotDesc);
+            umma_commit_warp(&s_full[ti]);
+            if (j + 2 == n_i) umma_commit_warp(&q_empty[ti]);  // that was the last S of Q_ti
+          } else {
+            umma_commit_warp(&o_full[ti]);
+          }
         }
         if (!ok) break;
-        umma_commit(&kv_empty[g % NS]);
-        for (int j = 0; j < nmax; ++j) {
-          const int gv = g + 2 * j + 1, gk = g + 2 * j + 2;
-          const bool next = j + 1 < nmax;
-          if (!mbar_wait(&kv_full[gv % NS], (gv / NS) & 1, ctl) ||
-              (next && !mbar_wait(&kv_full[gk % NS], (gk / NS) & 1, ctl))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          for (int ti = 0; ti < 2; ++ti) {
-            const int n_i = ti ? w.n1 : w.n0;
-            if (j >= n_i) continue;
-            if (!mbar_wait(&p_full[ti], n_p[ti] & 1, ctl)) {
-              ok = false;
-              break;
-            }
-            ++n_p[ti];
-            tc_fence_after();
-            const uint32_t sc = ti ? C::S_COL1 : C::S_COL0;
-            const uint32_t oc = ti ? C::O_COL1 : C::O_COL0;
-            bf16_issue_pv<D>(tmem + oc, tmem + sc, kvb + (gv % NS) * C::TILE_BYTES,
-                             j > 0 ? 1u : 0u);
-            if (j + 1 < n_i) {
-              bf16_issue_s<D>(tmem + sc, qb[ti], kvb + (gk % NS) * C::TILE_BYTES);
-              umma_commit(&s_full[ti]);
-              if (j + 2 == n_i) umma_commit(&q_empty[ti]);  // that was the last S of Q_ti
-            } else {
-              umma_commit(&o_full[ti]);
-            }
-          }
-          if (!ok) break;
-          umma_commit(&kv_empty[gv % NS]);
-          if (next) umma_commit(&kv_empty[gk % NS]);
-        }
-        g += 2 * nmax;
+        umma_commit_warp(&kv_empty[gv % NS]);
+        if (next) umma_commit_warp(&kv_empty[gk % NS]);
       }
-      // every MMA issued so far must finish before TMEM and shared memory are released
-      umma_commit(mma_done);
-      mbar_wait_drain(mma_done, 0, ctl);
+      g += 2 * nmax;
     }
+    // every MMA issued so far must finish before TMEM and shared memory are released
+    umma_commit_warp(mma_done);
+    mbar_wait_drain(mma_done, 0, ctl);
   } else {
     // ------------------------------------------------------------ TMA producer
+    // Whole warp, one elected lane issues (operands stay warp-uniform).
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      uint32_t n_q[2] = {0, 0};
-      int g = 0;  // ring positions issued
-      bool ok = true;
-      SeqCursor cur;
-      WorkTile w;
-      // one K or V tile into the next ring slot
-      auto load_kv = [&](int t) -> bool {
-        const int s = g % NS, u = g / NS;
-        if (u > 0 && !mbar_wait(&kv_empty[s], (u - 1) & 1, ctl)) return false;
-        mbar_arrive_expect_tx(&kv_full[s], C::TILE_BYTES);
+    }
+    __syncwarp();
+    uint32_t n_q[2] = {0, 0};
+    int g = 0;  // ring positions issued
+    bool ok = true;
+    SeqCursor cur;
+    WorkTile w;
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl));
+    };
+    const uint32_t kv_smem = smem_base + C::KV_OFF;
+    // one K or V tile into the next ring slot
+    auto load_kv = [&](int t) -> bool {
+      const int s = g % NS, u = g / NS;
+      if (u > 0 && !wait(&kv_empty[s], (u - 1) & 1)) return false;
+      mbar_arrive_expect_tx_warp(&kv_full[s], C::TILE_BYTES);
+#pragma unroll
+      for (int c = 0; c < C::NCHUNK; ++c)
+        tma_load_3d_warp(kv_smem + s * C::TILE_BYTES + c * C::CHUNK_BYTES, (t & 1) ? &tmV : &tmK,
+                         smem_u32(&kv_full[s]), c * 64, w.row_base + (t >> 1) * C::BN, w.plane);
+      ++g;
+      return true;
+    };
+    for (int it = 0; ok; ++it) {
+      const int step = bf16_tile(p, it, cur, w);
+      if (step == kTileEnd) break;
+      if (step == kTileSkip) continue;
+      const int nkv = 2 * max(w.n0, w.n1);
+      // K_0 and V_0 first: their slots are freed by the previous tile alone
+      const int head = min(2, nkv);
+      for (int t = 0; ok && t < head; ++t) ok = load_kv(t);
+      for (int ti = 0; ok && ti < 2; ++ti) {
+        if ((ti ? w.n1 : w.n0) == 0) continue;
+        if (n_q[ti] > 0 && !wait(&q_empty[ti], (n_q[ti] - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx_warp(&q_full[ti], C::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(smem + C::KV_OFF + s * C::TILE_BYTES + c * C::CHUNK_BYTES,
-                      (t & 1) ? &tmV : &tmK, &kv_full[s], c * 64, w.row_base + (t >> 1) * C::BN,
-                      w.plane);
-        ++g;
-        return true;
-      };
-      for (int it = 0; ok; ++it) {
-        const int step = bf16_tile(p, it, cur, w);
-        if (step == kTileEnd) break;
-        if (step == kTileSkip) continue;
-        const int nkv = 2 * max(w.n0, w.n1);
-        // K_0 and V_0 first: their slots are freed by the previous tile alone
-        const int head = min(2, nkv);
-        for (int t = 0; ok && t < head; ++t) ok = load_kv(t);
-        for (int ti = 0; ok && ti < 2; ++ti) {
-          if ((ti ? w.n1 : w.n0) == 0) continue;
-          if (n_q[ti] > 0 && !mbar_wait(&q_empty[ti], (n_q[ti] - 1) & 1, ctl)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&q_full[ti], C::TILE_BYTES);
-#pragma unroll
-          for (int c = 0; c < C::NCHUNK; ++c)
-            tma_load_3d(smem + C::Q_OFF + ti * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ,
-                        &q_full[ti], c * 64, w.row_base + w.qblk * 256 + 128 * ti, w.plane);
-          ++n_q[ti];
-        }
-        for (int t = head; ok && t < nkv; ++t) ok = load_kv(t);
+          tma_load_3d_warp(smem_base + C::Q_OFF + ti * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ,
+                           smem_u32(&q_full[ti]), c * 64, w.row_base + w.qblk * 256 + 128 * ti,
+                           w.plane);
+        ++n_q[ti];
       }
-      // drain: every copy issued must land before the CTA may exit
-      for (int ti = 0; ti < 2; ++ti)
-        if (n_q[ti] > 0) mbar_wait_drain(&q_full[ti], (n_q[ti] - 1) & 1, ctl);
-      for (int t = max(0, g - NS); t < g; ++t)
-        mbar_wait_drain(&kv_full[t % NS], (t / NS) & 1, ctl);
+      for (int t = head; ok && t < nkv; ++t) ok = load_kv(t);
     }
+    // drain: every copy issued must land before the CTA may exit
+    for (int ti = 0; ti < 2; ++ti)
+      if (n_q[ti] > 0) mbar_wait_drain(&q_full[ti], (n_q[ti] - 1) & 1, ctl);
+    for (int t = max(0, g - NS); t < g; ++t)
+      mbar_wait_drain(&kv_full[t % NS], (t / NS) & 1, ctl);
   }
 
   tc_fence_before();
