@@ -447,6 +447,8 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t sc = ti ? C::S_COL1 : C::S_COL0;
           const uint32_t oc = ti ? C::O_COL1 : C::O_COL0;
           bf16_issue_pv<D>(tmem + oc, tmem + sc, vd0 + (gv % NS) * kSlotDesc, j > 0 ? 1u : 0u);
+          // V_j is free for the producer as soon as its last reader is done
+          if (ti == ((j < w.n1) ? 1 : 0)) umma_commit_warp(&kv_empty[gv % NS]);
           if (j + 1 < n_i) {
             bf16_issue_s<D>(tmem + sc, qd[ti], kd0 + (gk % NS) * kSlotDesc);
             umma_commit_warp(&s_full[ti]);
@@ -456,7 +458,6 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
         if (!ok) break;
-        umma_commit_warp(&kv_empty[gv % NS]);
         if (next) umma_commit_warp(&kv_empty[gk % NS]);
       }
       g += 2 * nmax;
