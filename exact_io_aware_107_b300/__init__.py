@@ -33,7 +33,7 @@ def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens=None, out=No
                       stream=None):
     """O and LSE of softmax(scale * Q K^T + causal mask) V.
 
-    q, k, v: CUDA tensors, bf16 (D in {64, 128}) or fp32 (D <= 128), contiguous,
+    q, k, v: CUDA tensors, bf16 or fp16 (D in {64, 128}) or fp32 (D <= 128), contiguous,
     (B, H, N, D), or (H, N_total, D) with ``cu_seqlens`` (int32 CUDA tensor of
     nseq+1 offsets).  Returns (O, LSE) with O like q and LSE fp32 (B, H, N) or
     (H, N_total).  Enqueued on ``stream`` (default: torch's current stream).
@@ -71,11 +71,14 @@ def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens=None, out=No
     if q.dtype == torch.bfloat16:
         rc = _binding.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, D,
                                _ptr(cu_seqlens), causal, scale, handle)
+    elif q.dtype == torch.float16:
+        rc = _binding.attn_fwd_f16(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, D,
+                                   _ptr(cu_seqlens), causal, scale, handle)
     elif q.dtype == torch.float32:
         rc = _binding.attn_fwd_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, D,
                                    _ptr(cu_seqlens), causal, scale, handle)
     else:
-        raise TypeError("dtype must be bfloat16 or float32")
+        raise TypeError("dtype must be bfloat16, float16 or float32")
     if rc != _binding.ATTN_OK:
         raise AttnError(rc, "attention_forward")
     return out, lse

@@ -32,6 +32,8 @@ ATTN_ERR_SCALE = -9
 _SIGNATURES = {
     "attn_fwd": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4
                  + [ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p]),
+    "attn_fwd_f16": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4
+                     + [ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p]),
     "attn_fwd_f32": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4
                      + [ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p]),
     "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -77,6 +79,12 @@ def attn_fwd(q, k, v, o, lse, B, H, N, D, cu_seqlens, causal, scale, stream) -> 
     """bf16 forward; pointers are ints (device addresses) or None."""
     return load().attn_fwd(q, k, v, o, lse, int(B), int(H), int(N), int(D), cu_seqlens,
                            int(causal), float(scale), stream)
+
+
+def attn_fwd_f16(q, k, v, o, lse, B, H, N, D, cu_seqlens, causal, scale, stream) -> int:
+    """fp16 forward; pointers are ints (device addresses) or None."""
+    return load().attn_fwd_f16(q, k, v, o, lse, int(B), int(H), int(N), int(D), cu_seqlens,
+                               int(causal), float(scale), stream)
 
 
 def attn_fwd_f32(q, k, v, o, lse, B, H, N, D, cu_seqlens, causal, scale, stream) -> int:

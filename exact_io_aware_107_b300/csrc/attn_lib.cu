@@ -87,9 +87,16 @@ int prepare_device(DeviceState** out) {
   }
   if (st.checked < 0) return ATTN_ERR_ARCH;
   if (!st.attrs_set) {
-    if (cudaFuncSetAttribute(attn_fwd_bf16_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_fwd_bf16_kernel<64, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Bf16Cfg<64>::SMEM_ALLOC) != cudaSuccess ||
-        cudaFuncSetAttribute(attn_fwd_bf16_kernel<128>,
+        cudaFuncSetAttribute(attn_fwd_bf16_kernel<128, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Bf16Cfg<128>::SMEM_ALLOC) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_fwd_bf16_kernel<64, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Bf16Cfg<64>::SMEM_ALLOC) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_fwd_bf16_kernel<128, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Bf16Cfg<128>::SMEM_ALLOC) != cudaSuccess) {
       cudaGetLastError();
@@ -128,14 +135,16 @@ int check_common(const void* q, const void* k, const void* v, const void* o, con
   return ATTN_OK;
 }
 
-int encode_bf16_map(CUtensorMap* map, const void* base, int D, int rows, int planes) {
+int encode_16bit_map(CUtensorMap* map, const void* base, int D, int rows, int planes, bool f16) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(planes)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                                  static_cast<cuuint64_t>(rows) * D * 2};
   const cuuint32_t box[3] = {64, 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+  const CUresult r = g_encode(map,
+                              f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              3, const_cast<void*>(base),
                               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -156,14 +165,12 @@ __global__ void wait_selftest_kernel(unsigned long long budget, unsigned int* er
   __syncthreads();
 }
 
-}  // namespace
-}  // namespace attn
 
-using namespace attn;
 
-extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                        int H, int N, int D, const int* cu_seqlens, int causal, float scale,
-                        void* stream) {
+// Shared body of the two 16-bit entry points (bf16 and fp16).
+int fwd_16bit(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int N, int D, const int* cu_seqlens, int causal, float scale, void* stream,
+              bool f16) {
   int rc = check_common(q, k, v, o, lse, B, H, N, D, cu_seqlens, scale);
   if (rc != ATTN_OK) return rc;
   if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
@@ -174,13 +181,13 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
 
   const int planes = cu_seqlens ? H : B * H;
   CUtensorMap mq, mk, mv;
-  if (encode_bf16_map(&mq, q, D, N, planes) != ATTN_OK ||
-      encode_bf16_map(&mk, k, D, N, planes) != ATTN_OK ||
-      encode_bf16_map(&mv, v, D, N, planes) != ATTN_OK)
+  if (encode_16bit_map(&mq, q, D, N, planes, f16) != ATTN_OK ||
+      encode_16bit_map(&mk, k, D, N, planes, f16) != ATTN_OK ||
+      encode_16bit_map(&mv, v, D, N, planes, f16) != ATTN_OK)
     return ATTN_ERR_LAUNCH;
 
   Bf16Params p;
-  p.o = static_cast<__nv_bfloat16*>(o);
+  p.o = o;
   p.lse = lse;
   p.cu_seqlens = cu_seqlens;
   p.nseq = cu_seqlens ? B : 0;
@@ -198,15 +205,41 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   p.timeout_ns = g_timeout_ns.load();
   p.err = st->err;
 
-  const long long grid = std::min<long long>(items, st->sms);
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(items, st->sms));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (D == 64)
-    attn_fwd_bf16_kernel<64><<<static_cast<unsigned>(grid), Bf16Cfg<64>::THREADS,
-                               Bf16Cfg<64>::SMEM_ALLOC, s>>>(mq, mk, mv, p);
-  else
-    attn_fwd_bf16_kernel<128><<<static_cast<unsigned>(grid), Bf16Cfg<128>::THREADS,
-                                Bf16Cfg<128>::SMEM_ALLOC, s>>>(mq, mk, mv, p);
+  if (D == 64) {
+    if (f16)
+      attn_fwd_bf16_kernel<64, true><<<grid, Bf16Cfg<64>::THREADS, Bf16Cfg<64>::SMEM_ALLOC, s>>>(
+          mq, mk, mv, p);
+    else
+      attn_fwd_bf16_kernel<64, false><<<grid, Bf16Cfg<64>::THREADS, Bf16Cfg<64>::SMEM_ALLOC, s>>>(
+          mq, mk, mv, p);
+  } else {
+    if (f16)
+      attn_fwd_bf16_kernel<128, true><<<grid, Bf16Cfg<128>::THREADS, Bf16Cfg<128>::SMEM_ALLOC,
+                                        s>>>(mq, mk, mv, p);
+    else
+      attn_fwd_bf16_kernel<128, false><<<grid, Bf16Cfg<128>::THREADS, Bf16Cfg<128>::SMEM_ALLOC,
+                                         s>>>(mq, mk, mv, p);
+  }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int N, int D, const int* cu_seqlens, int causal, float scale,
+                        void* stream) {
+  return attn::fwd_16bit(q, k, v, o, lse, B, H, N, D, cu_seqlens, causal, scale, stream, false);
+}
+
+extern "C" int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int H, int N, int D, const int* cu_seqlens, int causal,
+                            float scale, void* stream) {
+  return attn::fwd_16bit(q, k, v, o, lse, B, H, N, D, cu_seqlens, causal, scale, stream, true);
 }
 
 extern "C" int attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,

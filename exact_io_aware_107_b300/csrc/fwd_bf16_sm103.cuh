@@ -1,5 +1,7 @@
-// bf16 attention forward for sm_103a: persistent CTAs, TMA + mbarrier
-// pipeline, tcgen05 MMAs with TMEM accumulators, online softmax in base 2.
+// 16-bit (bf16 or fp16) attention forward for sm_103a: persistent CTAs, TMA +
+// mbarrier pipeline, tcgen05 MMAs with TMEM accumulators, online softmax in
+// base 2.  The element type only changes the MMA instruction descriptor, the
+// TMA element type (set by the host) and the rounding of P and O.
 //
 // What it computes is the exact scaled-dot-product attention forward
 // O = softmax(scale * Q K^T + causal mask) V together with the per-row
@@ -50,7 +52,7 @@
 namespace attn {
 
 struct Bf16Params {
-  __nv_bfloat16* o;
+  void* o;                // bf16 or fp16 output, same layout as q
   float* lse;
   const int* cu_seqlens;  // nullptr for the dense layout
   int nseq;               // packed layout: number of sequences
@@ -177,10 +179,10 @@ __device__ __forceinline__ int bf16_tile(const Bf16Params& p, int it, SeqCursor&
 // descriptors of the tiles' first bytes; the start-address field (bits 0-13,
 // bytes / 16) is advanced in place, which cannot carry out of the field
 // because shared addresses stay below 256 KB.
-template <int D>
+template <int D, bool F16>
 __device__ __forceinline__ void bf16_issue_s(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
   using C = Bf16Cfg<D>;
-  constexpr uint32_t idesc = idesc_bf16_f32(128, C::BN, 0, 0);
+  constexpr uint32_t idesc = idesc_bf16_f32(128, C::BN, 0, 0, F16);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = ((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
@@ -189,11 +191,11 @@ __device__ __forceinline__ void bf16_issue_s(uint32_t d_tmem, uint64_t q_desc, u
 }
 
 // O (+)= P V: P (bf16 pairs) from TMEM columns p_tmem.., V tile from v_desc.
-template <int D>
+template <int D, bool F16>
 __device__ __forceinline__ void bf16_issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                               uint32_t accumulate) {
   using C = Bf16Cfg<D>;
-  constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
+  constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1, F16);
 #pragma unroll
   for (int kk = 0; kk < C::BN / 16; ++kk) {
     // V is the MN-major B operand: 16 keys = two 8-row groups of 128-byte rows
@@ -202,7 +204,7 @@ __device__ __forceinline__ void bf16_issue_pv(uint32_t d_tmem, uint32_t p_tmem, 
   }
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(320, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(320, 1)
           const float a = ex2_approx(lo_f32(x2));
           const float b = ex2_approx(hi_f32(x2));
           acc2[c & 1] = fadd2(acc2[c & 1], f32x2(a, b));
-          pk[c] = pack_bf16x2(a, b);
+          pk[c] = pack_16x2<F16>(a, b);
         }
         const uint64_t sum2 = fadd2(acc2[0], acc2[1]);
         l = l * alpha + (lo_f32(sum2) + hi_f32(sum2));
@@ -366,7 +368,7 @@ __global__ void __launch_bounds__(320, 1)
       const bool valid = row < w.seq_len;
       const size_t grow = static_cast<size_t>(w.plane) * p.rows + w.row_base + row;
       const float inv_l = 1.f / l;
-      uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + grow * D);
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -374,8 +376,8 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t h[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          h[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
-                             __uint_as_float(o[2 * e + 1]) * inv_l);
+          h[e] = pack_16x2<F16>(__uint_as_float(o[2 * e]) * inv_l,
+                                __uint_as_float(o[2 * e + 1]) * inv_l);
         if (valid) {
 #pragma unroll
           for (int v = 0; v < 4; ++v)
@@ -420,7 +422,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         ++n_q[ti];
         tc_fence_after();
-        bf16_issue_s<D>(tmem + (ti ? C::S_COL1 : C::S_COL0), qd[ti], k0);
+        bf16_issue_s<D, F16>(tmem + (ti ? C::S_COL1 : C::S_COL0), qd[ti], k0);
         umma_commit_warp(&s_full[ti]);
         if (n_i == 1) umma_commit_warp(&q_empty[ti]);
       }
@@ -446,11 +448,11 @@ __global__ void __launch_bounds__(320, 1)
           tc_fence_after();
           const uint32_t sc = ti ? C::S_COL1 : C::S_COL0;
           const uint32_t oc = ti ? C::O_COL1 : C::O_COL0;
-          bf16_issue_pv<D>(tmem + oc, tmem + sc, vd0 + (gv % NS) * kSlotDesc, j > 0 ? 1u : 0u);
+          bf16_issue_pv<D, F16>(tmem + oc, tmem + sc, vd0 + (gv % NS) * kSlotDesc, j > 0 ? 1u : 0u);
           // V_j is free for the producer as soon as its last reader is done
           if (ti == ((j < w.n1) ? 1 : 0)) umma_commit_warp(&kv_empty[gv % NS]);
           if (j + 1 < n_i) {
-            bf16_issue_s<D>(tmem + sc, qd[ti], kd0 + (gk % NS) * kSlotDesc);
+            bf16_issue_s<D, F16>(tmem + sc, qd[ti], kd0 + (gk % NS) * kSlotDesc);
             umma_commit_warp(&s_full[ti]);
             if (j + 2 == n_i) umma_commit_warp(&q_empty[ti]);  // that was the last S of Q_ti
           } else {

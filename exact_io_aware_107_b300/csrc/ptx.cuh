@@ -156,12 +156,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator.
+// Instruction descriptor for kind::f16 with 16-bit A/B (bf16, or fp16 when
+// f16 is set) and an fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_major,
-                                                      int b_mn_major) {
+                                                      int b_mn_major, bool f16 = false) {
   return (1u << 4)                                   // D = f32
-         | (1u << 7)                                 // A = bf16
-         | (1u << 10)                                // B = bf16
+         | ((f16 ? 0u : 1u) << 7)                    // A = bf16 (1) or f16 (0)
+         | ((f16 ? 0u : 1u) << 10)                   // B likewise
          | (static_cast<uint32_t>(a_mn_major) << 15) //
          | (static_cast<uint32_t>(b_mn_major) << 16) //
          | (static_cast<uint32_t>(N >> 3) << 17)     //
@@ -350,6 +351,17 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  // cvt.rn.f16x2.f32 d, a, b puts a in the upper half and b in the lower half.
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// Two fp32 values rounded to the kernel's 16-bit type (fp16 or bf16), packed.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_16x2(float lo, float hi);
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   // cvt.rn.bf16x2.f32 d, a, b puts a in the upper half and b in the lower half.
   uint32_t d;
@@ -404,6 +416,15 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("mul.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
+}
+
+template <>
+__device__ __forceinline__ uint32_t pack_16x2<false>(float lo, float hi) {
+  return pack_bf16x2(lo, hi);
+}
+template <>
+__device__ __forceinline__ uint32_t pack_16x2<true>(float lo, float hi) {
+  return pack_f16x2(lo, hi);
 }
 
 }  // namespace attn

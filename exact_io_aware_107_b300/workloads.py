@@ -37,7 +37,7 @@ import numpy as np
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    dtype: str            # "f32" or "bf16"
+    dtype: str            # "f32", "bf16" or "f16"
     B: int                # batch (number of sequences for varlen)
     H: int
     N: int                # seq_len (total tokens for varlen)
@@ -69,7 +69,7 @@ class Workload:
 
     def hbm_bytes(self) -> float:
         """Algorithmic HBM bytes: Q, K, V read once, O and LSE written once."""
-        elt = 2 if self.dtype == "bf16" else 4
+        elt = 4 if self.dtype == "f32" else 2
         rows = self.H * self.N if self.varlen is not None else self.B * self.H * self.N
         return 4.0 * rows * self.D * elt + rows * 4.0
 
@@ -121,6 +121,12 @@ def cu_seqlens_of(lengths) -> np.ndarray:
     return out
 
 
+def _round_f16(x32: np.ndarray):
+    """fp32 -> IEEE fp16 with round-to-nearest-even."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x32)).to(torch.float16)
+
+
 def _round_bf16(x32: np.ndarray):
     """fp32 -> bf16 with round-to-nearest-even (torch's conversion)."""
     import torch
@@ -156,6 +162,8 @@ def generate(w: Workload, as_torch=True):
         k *= np.float32(w.qk_std)
     if w.dtype == "bf16":
         tq, tk, tv = _round_bf16(q), _round_bf16(k), _round_bf16(v)
+    elif w.dtype == "f16":
+        tq, tk, tv = _round_f16(q), _round_f16(k), _round_f16(v)
     else:
         tq, tk, tv = (torch.from_numpy(np.ascontiguousarray(a)) for a in (q, k, v))
     cu = cu_seqlens_of(w.varlen) if w.varlen is not None else None

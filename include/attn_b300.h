@@ -80,6 +80,17 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              int N, int D, const int* cu_seqlens, int causal, float scale, void* stream);
 
 /*
+ * fp16 forward on tcgen05 tensor cores: the same as attn_fwd with IEEE
+ * half-precision q, k, v and o (__half).  The probabilities are rounded to
+ * fp16 for the second product and O is rounded to fp16 once at the end; the
+ * rest of the arithmetic is as in attn_fwd.  This is the "mixed precision
+ * fp16" variant named by "Build a FlashAttention kernel from scratch with
+ * Python and NumPy" (section "Extending It", mixed-precision support).
+ */
+int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int D, const int* cu_seqlens, int causal, float scale, void* stream);
+
+/*
  * fp32 forward on CUDA cores: same arguments and layouts with float tensors
  * (16-byte aligned), 1 <= D <= 128.  Scores, probabilities and accumulators
  * stay in fp32; exponentials use the accurate expf.

@@ -45,7 +45,7 @@ def test_version_and_strerror(lib):
 P = 1 << 20  # a 16-byte aligned stand-in address; never dereferenced on these paths
 
 
-@pytest.mark.parametrize("fn", [B.attn_fwd, B.attn_fwd_f32])
+@pytest.mark.parametrize("fn", [B.attn_fwd, B.attn_fwd_f16, B.attn_fwd_f32])
 def test_argument_errors_return_before_launch(lib, fn):
     good = dict(q=P, k=P, v=P, o=P, lse=P, B=1, H=1, N=16, D=64, cu_seqlens=None, causal=1,
                 scale=0.125, stream=None)
@@ -73,9 +73,10 @@ def test_argument_errors_return_before_launch(lib, fn):
     assert call(N=0, q=None, k=None, v=None, o=None, lse=None) == B.ATTN_OK
 
 
-def test_bf16_head_dims(lib):
-    for d in (32, 96, 256):
-        assert B.attn_fwd(P, P, P, P, P, 1, 1, 16, d, None, 1, 0.1, None) == B.ATTN_ERR_HEADDIM
+def test_16bit_head_dims(lib):
+    for fn in (B.attn_fwd, B.attn_fwd_f16):
+        for d in (32, 96, 256):
+            assert fn(P, P, P, P, P, 1, 1, 16, d, None, 1, 0.1, None) == B.ATTN_ERR_HEADDIM
 
 
 def test_timeout_setter(lib):
@@ -90,4 +91,5 @@ def test_no_device_means_loud_failure(lib):
         pytest.skip("a CUDA device is present")
     # valid arguments with no GPU: the call fails, it never computes on the CPU
     assert B.attn_fwd(P, P, P, P, P, 1, 1, 16, 64, None, 1, 0.125, None) == B.ATTN_ERR_LAUNCH
+    assert B.attn_fwd_f16(P, P, P, P, P, 1, 1, 16, 64, None, 1, 0.125, None) == B.ATTN_ERR_LAUNCH
     assert B.attn_fwd_f32(P, P, P, P, P, 1, 1, 16, 64, None, 1, 0.125, None) == B.ATTN_ERR_LAUNCH

@@ -15,7 +15,7 @@ def _gen(dtype, B, H, N, D, seed, causal=True):
     return x["q"], x["k"], x["v"]
 
 
-@pytest.mark.parametrize("dtype,D", [("bf16", 64), ("bf16", 128), ("f32", 64)])
+@pytest.mark.parametrize("dtype,D", [("bf16", 64), ("bf16", 128), ("f16", 128), ("f32", 64)])
 def test_causal_row0_is_v0_bit_exact(dtype, D):
     q, k, v = _gen(dtype, 2, 3, 333, D, 1)
     o, lse = run_cuda(q, k, v, True, 0.125)
@@ -39,7 +39,7 @@ def test_future_keys_do_not_leak(dtype, D):
     assert np.abs(o1[:, :, i + 1:] - o2[:, :, i + 1:]).max() > 1e-2
 
 
-@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("bf16", 64), ("f32", 64)])
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("bf16", 64), ("f16", 128), ("f32", 64)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_packed_equals_dense_per_sequence(dtype, D, causal):
     lens = [5, 128, 300, 1, 257, 640]

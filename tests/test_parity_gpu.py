@@ -10,7 +10,8 @@ import pytest
 
 import oracle
 from exact_io_aware_107_b300 import workloads as W
-from gpu_util import (BF16_TOL_LSE, BF16_TOL_O, F32_TOL_LSE, F32_TOL_O, max_err, run_cuda)
+from gpu_util import (BF16_TOL_LSE, BF16_TOL_O, F16_TOL_LSE, F16_TOL_O, F32_TOL_LSE, F32_TOL_O,
+                      max_err, run_cuda)
 
 pytestmark = pytest.mark.gpu
 
@@ -94,6 +95,43 @@ def test_bf16_growing_max_forces_rescale():
         o, lse = run_cuda(tq, tk, tv, causal, scale)
         ro, rl = oracle.attention(W.as_f64(tq), W.as_f64(tk), W.as_f64(tv), scale, causal)
         assert max_err(o, ro) <= BF16_TOL_O and max_err(lse, rl) <= BF16_TOL_LSE
+
+
+# ---------------------------------------------------------------- fp16 path
+
+@pytest.mark.parametrize("N", [1, 7, 128, 129, 300, 700])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_f16_sweep(N, D, causal):
+    w = W.custom("f16", B=1, H=2, N=N, D=D, causal=causal, seed=N * 5 + D)
+    _full_compare(w, F16_TOL_O, F16_TOL_LSE)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_f16_varlen_small(causal):
+    w = W.custom("f16", H=3, D=128, causal=causal, seed=19, varlen=[1, 127, 129, 300, 513])
+    _full_compare(w, F16_TOL_O, F16_TOL_LSE)
+
+
+def test_f16_peaked_small():
+    w = W.custom("f16", B=1, H=4, N=1500, D=128, causal=True, seed=23, qk_std=2.0)
+    _full_compare(w, F16_TOL_O, F16_TOL_LSE)
+
+
+def test_f16_causal_b2_h32_n8192_d128_sampled():
+    w = W.custom("f16", B=2, H=32, N=8192, D=128, causal=True, seed=0,
+                 name="f16_causal_b2_h32_n8192_d128")
+    x = W.generate(w)
+    o, lse = run_cuda(x["q"], x["k"], x["v"], w.causal, w.scale)
+    rng = np.random.default_rng(5)
+    worst_o = worst_l = 0.0
+    for b, h in ((0, 0), (1, 31), (0, 17)):
+        rows = _sample_rows(w.N, rng)
+        ro, rl = oracle.attention_rows(W.as_f64(x["q"][b, h]), W.as_f64(x["k"][b, h]),
+                                       W.as_f64(x["v"][b, h]), w.scale, w.causal, rows)
+        worst_o = max(worst_o, max_err(o[b, h][rows], ro))
+        worst_l = max(worst_l, max_err(lse[b, h][rows], rl))
+    assert worst_o <= F16_TOL_O and worst_l <= F16_TOL_LSE, (worst_o, worst_l)
 
 
 # ---------------------------------------------------------------- the named workloads
