@@ -411,6 +411,63 @@ def run_ours(args, w):
     return 0
 
 
+def run_decode(args):
+    """KV-cache decode (a NEXT row): device-timed GB/s against the HBM roofline."""
+    import torch
+    from exact_io_aware_107_b300 import _binding, attention_decode, device_error
+
+    ws_, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    B, H, Nq, Nk, D = (int(t) for t in args.decode_shape.split(","))
+    rng = np.random.default_rng(0)
+    def draw(*shape):
+        return torch.from_numpy(rng.standard_normal(shape, dtype=np.float32)).to(torch.bfloat16)
+    q, k, v = draw(B, H, Nq, D), draw(B, H, Nk, D), draw(B, H, Nk, D)
+    dev = torch.device("cuda", local)
+    dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+    rc, nbytes = _binding.attn_decode_workspace_bytes(B, H, Nq, Nk, D)
+    assert rc == 0
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(dq)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        attention_decode(dq, dk, dv, workspace=ws, out=o, lse=lse, stream=stream)
+    torch.cuda.synchronize()
+    assert device_error() == 0
+    with ClockSampler(local) as clk:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            attention_decode(dq, dk, dv, workspace=ws, out=o, lse=lse, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    assert device_error() == 0
+    ms = e0.elapsed_time(e1) / args.steps
+    nbytes_alg = 2 * B * H * Nk * D * 2 + 2 * B * H * Nq * D * 2 + B * H * Nq * 4
+    _, hbm_peak, kind = load_peaks()
+    gbs = nbytes_alg / (ms * 1e-3) / 1e9
+    line = {
+        "metric": "attention decode GB/s (bf16, KV cache, non-causal)", "value": gbs,
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"decode_b{B}_h{H}_nq{Nq}_nk{Nk}_d{D}", "B": B, "H": H, "Nq": Nq,
+                   "Nk": Nk, "D": D, "workspace_bytes": nbytes,
+                   "l2": "K/V larger than L2 (no flush)" if 2 * B * H * Nk * D * 2 > 126e6
+                   else "K/V fit in L2"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": gbs / hbm_peak, "peak_source": f"{kind} copy bandwidth",
+                     "kernel": f"attn_decode_bf16_kernel<{D}>", "traffic": None,
+                     "algorithmic_bytes": nbytes_alg},
+        "gpu_launches": args.steps * (2 if nbytes > 0 else 1),
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -419,11 +476,16 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["forward", "decode"], default="forward",
+                    help="decode: the KV-cache decode path (GB/s against HBM)")
+    ap.add_argument("--decode-shape", default="8,32,1,32768,128", help="B,H,Nq,Nk,D for --op decode")
     ap.add_argument("--shape", default=None,
                     help="B,H,N,D: same dtype and mask as --workload at another size "
                          "(profiling cases)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
+    if args.op == "decode":
+        return run_decode(args)
     w = W.WORKLOADS[args.workload]
     if args.shape:
         b, h, n, d = (int(t) for t in args.shape.split(","))

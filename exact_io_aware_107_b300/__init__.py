@@ -18,7 +18,7 @@ import math
 from . import _binding
 from ._binding import AttnError
 
-__all__ = ["attention_forward", "AttnError", "device_error", "load_library"]
+__all__ = ["attention_forward", "attention_decode", "AttnError", "device_error", "load_library"]
 
 
 def load_library():
@@ -81,6 +81,43 @@ def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens=None, out=No
         raise TypeError("dtype must be bfloat16, float16 or float32")
     if rc != _binding.ATTN_OK:
         raise AttnError(rc, "attention_forward")
+    return out, lse
+
+
+def attention_decode(q, k, v, scale=None, workspace=None, out=None, lse=None, stream=None):
+    """KV-cache decode: O and LSE of Nq new rows against all cached keys, no mask.
+
+    q: bf16 (B, H, Nq, D) with 1 <= Nq <= 8; k, v: bf16 (B, H, Nk, D) CUDA tensors.
+    ``workspace``: a CUDA tensor of at least ``decode_workspace_bytes`` bytes, or
+    None to let torch allocate one here (the library itself never allocates).
+    """
+    import torch
+
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16 or t.dim() != 4:
+            raise ValueError("q, k, v must be contiguous 4-D bf16 CUDA tensors")
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, D) or v.shape != k.shape:
+        raise ValueError("k, v must be (B, H, Nk, D) with q's B, H, D")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        rc, nbytes = _binding.attn_decode_workspace_bytes(B, H, Nq, Nk, D)
+        if rc != _binding.ATTN_OK:
+            raise AttnError(rc, "attention_decode")
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = _binding.attn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, D,
+                              scale, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              stream.cuda_stream)
+    if rc != _binding.ATTN_OK:
+        raise AttnError(rc, "attention_decode")
     return out, lse
 
 

@@ -36,6 +36,10 @@ _SIGNATURES = {
                      + [ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p]),
     "attn_fwd_f32": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4
                      + [ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p]),
+    "attn_decode": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
+                    + [ctypes.c_float, ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_void_p]),
+    "attn_decode_workspace_bytes": (ctypes.c_int, [ctypes.c_int] * 5
+                                    + [ctypes.POINTER(ctypes.c_ulonglong)]),
     "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_get_device_error": (ctypes.c_int, [ctypes.c_void_p]),
     "attn_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_ulonglong]),
@@ -91,6 +95,21 @@ def attn_fwd_f32(q, k, v, o, lse, B, H, N, D, cu_seqlens, causal, scale, stream)
     """fp32 forward; pointers are ints (device addresses) or None."""
     return load().attn_fwd_f32(q, k, v, o, lse, int(B), int(H), int(N), int(D), cu_seqlens,
                                int(causal), float(scale), stream)
+
+
+def attn_decode(q, k, v, o, lse, B, H, Nq, Nk, D, scale, workspace, workspace_bytes,
+                stream) -> int:
+    """bf16 KV-cache decode; pointers are ints (device addresses) or None."""
+    return load().attn_decode(q, k, v, o, lse, int(B), int(H), int(Nq), int(Nk), int(D),
+                              float(scale), workspace, int(workspace_bytes), stream)
+
+
+def attn_decode_workspace_bytes(B, H, Nq, Nk, D):
+    """(status, bytes) for the decode workspace on the current device."""
+    n = ctypes.c_ulonglong(0)
+    rc = load().attn_decode_workspace_bytes(int(B), int(H), int(Nq), int(Nk), int(D),
+                                            ctypes.byref(n))
+    return rc, n.value
 
 
 def attn_get_device_error(stream) -> int:

@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "../../include/attn_b300.h"
+#include "decode_bf16.cuh"
 #include "fwd_bf16_sm103.cuh"
 #include "fwd_f32.cuh"
 #include "ptx.cuh"
@@ -40,6 +41,27 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
+
+template <int D, int NQ>
+bool set_decode_smem() {
+  return cudaFuncSetAttribute(attn_decode_bf16_kernel<D, NQ>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              DecCfg<D>::SMEM_ALLOC) != cudaSuccess;
+}
+
+template <int D>
+void launch_decode_kernel(unsigned grid, cudaStream_t s, const CUtensorMap& mk,
+                          const CUtensorMap& mv, const DecodeParams& p) {
+  constexpr int T = DecCfg<D>::THREADS, SM = DecCfg<D>::SMEM_ALLOC;
+  if (p.nq <= 1)
+    attn_decode_bf16_kernel<D, 1><<<grid, T, SM, s>>>(mk, mv, p);
+  else if (p.nq <= 2)
+    attn_decode_bf16_kernel<D, 2><<<grid, T, SM, s>>>(mk, mv, p);
+  else if (p.nq <= 4)
+    attn_decode_bf16_kernel<D, 4><<<grid, T, SM, s>>>(mk, mv, p);
+  else
+    attn_decode_bf16_kernel<D, 8><<<grid, T, SM, s>>>(mk, mv, p);
+}
 
 // Checks the current device once and fetches what the launches need.
 int prepare_device(DeviceState** out) {
@@ -99,6 +121,12 @@ int prepare_device(DeviceState** out) {
         cudaFuncSetAttribute(attn_fwd_bf16_kernel<128, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Bf16Cfg<128>::SMEM_ALLOC) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_LAUNCH;
+    }
+    if (set_decode_smem<64, 1>() || set_decode_smem<64, 2>() || set_decode_smem<64, 4>() ||
+        set_decode_smem<64, 8>() || set_decode_smem<128, 1>() || set_decode_smem<128, 2>() ||
+        set_decode_smem<128, 4>() || set_decode_smem<128, 8>()) {
       cudaGetLastError();
       return ATTN_ERR_LAUNCH;
     }
@@ -225,10 +253,117 @@ int fwd_16bit(const void* q, const void* k, const void* v, void* o, float* lse, 
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
+// Key slices per plane for the decode kernel: enough CTAs to cover every SM
+// about twice (bandwidth needs many loads in flight), slices of whole tiles.
+struct DecodePlan {
+  int nsplit;
+  int chunk;
+  size_t ws_bytes;
+};
+
+DecodePlan plan_decode(int planes, int nq, int nk, int D, int sms) {
+  const int tiles = (nk + 127) / 128;
+  const int per_sm = (D == 64) ? 4 : 2;
+  long long want = (1LL * per_sm * sms + planes - 1) / planes;
+  want = std::max(1LL, std::min<long long>(want, tiles));
+  const int chunk = static_cast<int>((tiles + want - 1) / want) * 128;
+  const int nsplit = (nk + chunk - 1) / chunk;
+  DecodePlan d;
+  d.nsplit = nsplit;
+  d.chunk = chunk;
+  d.ws_bytes = nsplit > 1 ? static_cast<size_t>(planes) * nsplit * nq * (D + 1) * sizeof(float) : 0;
+  return d;
+}
+
+int check_decode(const void* q, const void* k, const void* v, const void* o, const void* lse,
+                 int B, int H, int Nq, int Nk, int D, float scale) {
+  if (B < 1 || H < 1 || Nq < 1 || Nq > kDecodeMaxQ || Nk < 1) return ATTN_ERR_SHAPE;
+  if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+  if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_SCALE;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4))
+    return ATTN_ERR_ALIGN;
+  const long long planes = 1LL * B * H;
+  if (planes > (1 << 24) || planes * Nk > (1LL << 40)) return ATTN_ERR_SHAPE;
+  return ATTN_OK;
+}
+
+// Launches the decode kernels with the given split plan and workspace.
+int launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                  int Nq, int Nk, int D, float scale, const DecodePlan& plan, float* ws,
+                  DeviceState* st, cudaStream_t s) {
+  const int planes = B * H;
+  CUtensorMap mk, mv;
+  if (encode_16bit_map(&mk, k, D, Nk, planes, false) != ATTN_OK ||
+      encode_16bit_map(&mv, v, D, Nk, planes, false) != ATTN_OK)
+    return ATTN_ERR_LAUNCH;
+  DecodeParams p;
+  p.o = o;
+  p.lse = lse;
+  p.ws_o = ws;
+  p.ws_lse = ws ? ws + static_cast<size_t>(planes) * plan.nsplit * Nq * D : nullptr;
+  p.q = q;
+  p.planes = planes;
+  p.nq = Nq;
+  p.nk = Nk;
+  p.nsplit = plan.nsplit;
+  p.chunk = plan.chunk;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = g_timeout_ns.load();
+  p.err = st->err;
+  const unsigned grid = static_cast<unsigned>(planes * plan.nsplit);
+  if (D == 64)
+    launch_decode_kernel<64>(grid, s, mk, mv, p);
+  else
+    launch_decode_kernel<128>(grid, s, mk, mv, p);
+  if (plan.nsplit > 1) {
+    const unsigned rows = static_cast<unsigned>(planes * Nq);
+    if (D == 64)
+      attn_decode_merge_kernel<64><<<rows, 64, 0, s>>>(p);
+    else
+      attn_decode_merge_kernel<128><<<rows, 128, 0, s>>>(p);
+  }
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
 }  // namespace
 }  // namespace attn
 
 using namespace attn;
+
+extern "C" int attn_decode_workspace_bytes(int B, int H, int Nq, int Nk, int D,
+                                           unsigned long long* bytes) {
+  if (!bytes) return ATTN_ERR_NULL;
+  if (B < 1 || H < 1 || Nq < 1 || Nq > kDecodeMaxQ || Nk < 1) return ATTN_ERR_SHAPE;
+  if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+  DeviceState* st = nullptr;
+  const int rc = prepare_device(&st);
+  if (rc != ATTN_OK) return rc;
+  *bytes = plan_decode(B * H, Nq, Nk, D, st->sms).ws_bytes;
+  return ATTN_OK;
+}
+
+extern "C" int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int Nq, int Nk, int D, float scale, void* workspace,
+                           unsigned long long workspace_bytes, void* stream) {
+  int rc = check_decode(q, k, v, o, lse, B, H, Nq, Nk, D, scale);
+  if (rc != ATTN_OK) return rc;
+  if (workspace && !aligned(workspace, 16)) return ATTN_ERR_ALIGN;
+  DeviceState* st = nullptr;
+  rc = prepare_device(&st);
+  if (rc != ATTN_OK) return rc;
+  DecodePlan plan = plan_decode(B * H, Nq, Nk, D, st->sms);
+  if (plan.nsplit > 1 && (workspace == nullptr || workspace_bytes < plan.ws_bytes)) {
+    // no (or too small a) workspace: one slice per plane, written directly
+    plan.nsplit = 1;
+    plan.chunk = ((Nk + 127) / 128) * 128;
+    plan.ws_bytes = 0;
+  }
+  return launch_decode(q, k, v, o, lse, B, H, Nq, Nk, D, scale, plan,
+                       plan.nsplit > 1 ? static_cast<float*>(workspace) : nullptr, st,
+                       static_cast<cudaStream_t>(stream));
+}
 
 extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int H, int N, int D, const int* cu_seqlens, int causal, float scale,

@@ -99,6 +99,35 @@ int attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float
                  int H, int N, int D, const int* cu_seqlens, int causal, float scale,
                  void* stream);
 
+/*
+ * KV-cache decode (bf16): Nq new query rows per (batch, head) attend to all Nk
+ * cached keys, without a mask -- the incremental-decoding call of "Python
+ * Attention Mechanisms Explained: From Self-Attention to Flash Attention"
+ * (section "Causal Masking and Incremental Decoding"): a query of length 1
+ * (here 1..8) against the key/value cache, is_causal=False.  Same definition of
+ * O and LSE as attn_fwd with J(i) = every cached key.
+ *   q : bf16 (B, H, Nq, D)        k, v : bf16 (B, H, Nk, D)
+ *   o : bf16 (B, H, Nq, D)        lse  : fp32 (B, H, Nq)
+ *   1 <= Nq <= 8, Nk >= 1, D in {64, 128}, scale finite and > 0.
+ * The keys of each plane are split across thread blocks and the partial
+ * results merged by their log-sum-exp.  The partials live in a caller-owned
+ * device workspace of attn_decode_workspace_bytes() bytes (16-byte aligned);
+ * with workspace == NULL (or too small) every plane is processed by one
+ * thread block instead, which is correct but slower for few planes.
+ * Arithmetic: bf16 operands, fp32 scores, probabilities, sums and outputs;
+ * O rounded to bf16 once.
+ */
+int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Nq, int Nk, int D, float scale, void* workspace,
+                unsigned long long workspace_bytes, void* stream);
+
+/*
+ * Workspace size attn_decode wants for this shape on the current device
+ * (0 when one thread block per plane is already enough).  Returns a status;
+ * the size goes to *bytes.
+ */
+int attn_decode_workspace_bytes(int B, int H, int Nq, int Nk, int D, unsigned long long* bytes);
+
 /* Static description of a status code. */
 const char* attn_strerror(int status);
 

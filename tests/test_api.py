@@ -93,3 +93,25 @@ def test_no_device_means_loud_failure(lib):
     assert B.attn_fwd(P, P, P, P, P, 1, 1, 16, 64, None, 1, 0.125, None) == B.ATTN_ERR_LAUNCH
     assert B.attn_fwd_f16(P, P, P, P, P, 1, 1, 16, 64, None, 1, 0.125, None) == B.ATTN_ERR_LAUNCH
     assert B.attn_fwd_f32(P, P, P, P, P, 1, 1, 16, 64, None, 1, 0.125, None) == B.ATTN_ERR_LAUNCH
+
+
+def test_decode_argument_errors(lib):
+    def call(**kw):
+        a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, H=2, Nq=1, Nk=100, D=128, scale=0.1, ws=None,
+                 wsb=0)
+        a.update(kw)
+        return B.attn_decode(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"],
+                             a["Nk"], a["D"], a["scale"], a["ws"], a["wsb"], None)
+    assert call(Nq=0) == B.ATTN_ERR_SHAPE
+    assert call(Nq=9) == B.ATTN_ERR_SHAPE
+    assert call(Nk=0) == B.ATTN_ERR_SHAPE
+    assert call(B=0) == B.ATTN_ERR_SHAPE
+    assert call(D=96) == B.ATTN_ERR_HEADDIM
+    assert call(scale=0.0) == B.ATTN_ERR_SCALE
+    assert call(v=None) == B.ATTN_ERR_NULL
+    assert call(o=P + 2) == B.ATTN_ERR_ALIGN
+    assert call(ws=P + 4, wsb=1024) == B.ATTN_ERR_ALIGN
+    rc, _ = B.attn_decode_workspace_bytes(1, 1, 9, 10, 128)
+    assert rc == B.ATTN_ERR_SHAPE
+    rc, _ = B.attn_decode_workspace_bytes(1, 1, 1, 10, 80)
+    assert rc == B.ATTN_ERR_HEADDIM

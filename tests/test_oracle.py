@@ -311,3 +311,40 @@ def test_mutants_are_caught(kind):
         except (AssertionError, FloatingPointError, ValueError):
             failed.append(pin.__name__)
     assert failed, f"mutant {kind} passed every pin"
+
+
+# ---------------------------------------------------------------------------
+# Rectangular (decode) form: fewer query rows than keys, no mask
+# ---------------------------------------------------------------------------
+
+def test_rectangular_noncausal_brute_force():
+    rng = np.random.default_rng(31)
+    for nq in (1, 2, 5):
+        for nk in (1, 3, 9):
+            q, k, v = _rand(rng, nq, 4), _rand(rng, nk, 4), _rand(rng, nk, 3)
+            o, lse = A.attention_plane(q, k, v, 0.6, False)
+            assert o.shape == (nq, 3) and lse.shape == (nq,)
+            for i in range(nq):
+                s = [0.6 * math.fsum(q[i, t] * k[j, t] for t in range(4)) for j in range(nk)]
+                mx = max(s)
+                e = [math.exp(x - mx) for x in s]
+                den = math.fsum(e)
+                for t in range(3):
+                    ref = math.fsum(e[j] * v[j, t] for j in range(nk)) / den
+                    assert abs(o[i, t] - ref) <= 1e-13 * (1 + abs(ref))
+                assert abs(lse[i] - (mx + math.log(den))) <= 1e-13 * (1 + abs(mx))
+
+
+def test_key_slices_merge_by_log_sum_exp():
+    # The split-key form: attention over key slices, merged with weights
+    # exp(LSE_c - LSE), LSE = ln sum_c exp(LSE_c), equals attention over all keys.
+    rng = np.random.default_rng(32)
+    q, k, v = _rand(rng, 3, 8), _rand(rng, 1000, 8), _rand(rng, 1000, 8)
+    o, lse = A.attention_plane(q, k, v, 0.4, False)
+    bounds = [0, 128, 129, 512, 999, 1000]
+    parts = [A.attention_plane(q, k[a:b], v[a:b], 0.4, False) for a, b in zip(bounds, bounds[1:])]
+    lses = np.stack([pl for _, pl in parts])
+    lse_m = np.log(np.exp(lses - lses.max(0)).sum(0)) + lses.max(0)
+    o_m = sum(np.exp(pl - lse_m)[:, None] * po for po, pl in parts)
+    np.testing.assert_allclose(lse_m, lse, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o_m, o, rtol=0, atol=1e-12)
