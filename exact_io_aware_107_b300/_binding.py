@@ -27,6 +27,8 @@ ATTN_ERR_LAUNCH = -6
 ATTN_ERR_TIMEOUT = -7
 ATTN_ERR_BOUNDS = -8
 ATTN_ERR_SCALE = -9
+ATTN_ERR_SCRATCH = -10
+NOALLOC_SCRATCH_BYTES = 2 << 20
 
 # Every symbol include/attn_b300.h declares, with its ctypes signature.
 _SIGNATURES = {
@@ -38,6 +40,8 @@ _SIGNATURES = {
                      + [ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p]),
     "attn_decode": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
                     + [ctypes.c_float, ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_void_p]),
+    "attn_decode_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
+                            + [ctypes.c_float, ctypes.c_void_p]),
     "attn_decode_workspace_bytes": (ctypes.c_int, [ctypes.c_int] * 5
                                     + [ctypes.POINTER(ctypes.c_ulonglong)]),
     "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -102,6 +106,12 @@ def attn_decode(q, k, v, o, lse, B, H, Nq, Nk, D, scale, workspace, workspace_by
     """bf16 KV-cache decode; pointers are ints (device addresses) or None."""
     return load().attn_decode(q, k, v, o, lse, int(B), int(H), int(Nq), int(Nk), int(D),
                               float(scale), workspace, int(workspace_bytes), stream)
+
+
+def attn_decode_noalloc(q, k, v, o, lse, B, H, Nq, Nk, D, scale, stream) -> int:
+    """Decode without a caller workspace (the library's built-in scratch is used)."""
+    return load().attn_decode_noalloc(q, k, v, o, lse, int(B), int(H), int(Nq), int(Nk), int(D),
+                                      float(scale), stream)
 
 
 def attn_decode_workspace_bytes(B, H, Nq, Nk, D):

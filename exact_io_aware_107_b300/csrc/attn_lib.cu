@@ -22,6 +22,12 @@ namespace attn {
 
 __device__ unsigned int g_dev_error;
 
+// Scratch of attn_decode_noalloc: the per-slice decode partials of one call
+// (see include/attn_b300.h).  Fixed size, one copy per device, shared by every
+// call of that entry point.
+constexpr size_t kNoAllocScratchBytes = ATTN_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) float g_decode_scratch[kNoAllocScratchBytes / sizeof(float)];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -344,6 +350,53 @@ extern "C" int attn_decode_workspace_bytes(int B, int H, int Nq, int Nk, int D,
   return ATTN_OK;
 }
 
+namespace {
+// Device address of g_decode_scratch, looked up once per device (with that
+// device current) by the first attn_decode_noalloc call on it.  In host code
+// the array's name only stands in for the symbol; it is not an address the
+// kernels may be given.
+float* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+int noalloc_scratch(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return ATTN_ERR_LAUNCH;
+    }
+    g_scratch_addr[dev] = static_cast<float*>(ptr);
+  }
+  *out = g_scratch_addr[dev];
+  return ATTN_OK;
+}
+}  // namespace
+
+extern "C" int attn_decode_noalloc(const void* q, const void* k, const void* v, void* o,
+                                   float* lse, int B, int H, int Nq, int Nk, int D, float scale,
+                                   void* stream) {
+  int rc = check_decode(q, k, v, o, lse, B, H, Nq, Nk, D, scale);
+  if (rc != ATTN_OK) return rc;
+  DeviceState* st = nullptr;
+  rc = prepare_device(&st);
+  if (rc != ATTN_OK) return rc;
+  const DecodePlan plan = plan_decode(B * H, Nq, Nk, D, st->sms);
+  if (plan.ws_bytes > kNoAllocScratchBytes) return ATTN_ERR_SCRATCH;
+  float* scratch = nullptr;
+  if (plan.nsplit > 1) {
+    rc = noalloc_scratch(&scratch);
+    if (rc != ATTN_OK) return rc;
+  }
+  return launch_decode(q, k, v, o, lse, B, H, Nq, Nk, D, scale, plan, scratch, st,
+                       static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse,
                            int B, int H, int Nq, int Nk, int D, float scale, void* workspace,
                            unsigned long long workspace_bytes, void* stream) {
@@ -420,6 +473,8 @@ extern "C" const char* attn_strerror(int status) {
     case ATTN_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out of time";
     case ATTN_ERR_BOUNDS: return "cu_seqlens entries outside [0, N] or decreasing";
     case ATTN_ERR_SCALE: return "scale must be finite and > 0";
+    case ATTN_ERR_SCRATCH:
+      return "decode partials need more than the built-in scratch (ATTN_NOALLOC_SCRATCH_BYTES)";
     default: return "unknown status";
   }
 }

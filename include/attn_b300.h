@@ -61,7 +61,9 @@ typedef enum {
   ATTN_ERR_LAUNCH = -6,   /* the CUDA runtime refused the launch or set-up              */
   ATTN_ERR_TIMEOUT = -7,  /* (device) a bounded wait inside a kernel ran out of time    */
   ATTN_ERR_BOUNDS = -8,   /* (device) cu_seqlens entries outside [0, N] or decreasing   */
-  ATTN_ERR_SCALE = -9     /* scale is not a finite number > 0                           */
+  ATTN_ERR_SCALE = -9,    /* scale is not a finite number > 0                           */
+  ATTN_ERR_SCRATCH = -10  /* attn_decode_noalloc: the problem needs more than the built-in
+                             scratch (ATTN_NOALLOC_SCRATCH_BYTES)                        */
 } attn_status;
 
 /*
@@ -127,6 +129,32 @@ int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse
  * the size goes to *bytes.
  */
 int attn_decode_workspace_bytes(int B, int H, int Nq, int Nk, int D, unsigned long long* bytes);
+
+/*
+ * attn_decode_noalloc: attn_decode for callers that cannot allocate device
+ * memory -- for example a host program embedded in another runtime that owns
+ * every byte of device memory through its own pool (a cudaMalloc from here
+ * would fail or fragment that pool), or latency-sensitive code that must not
+ * pay for the device-wide synchronisation that freeing memory implies.  It
+ * takes the same arguments as attn_decode except the workspace: the per-slice
+ * partial results go to a scratch array built into the library, of
+ * ATTN_NOALLOC_SCRATCH_BYTES per device, which every device that loads the
+ * library holds until the process exits.  The call allocates nothing.
+ *   - A problem whose partials need more than that returns ATTN_ERR_SCRATCH
+ *     without launching (attn_decode_workspace_bytes gives the need).
+ *   - The first call on a device looks up the array's device address; make
+ *     that first call before any stream capture.
+ *   - Every call uses the same array and leaves its partials there; each call
+ *     writes every entry it later reads, so nothing has to start at zero, but
+ *     two calls that run on the GPU at the same time (different streams, or
+ *     different host threads) overwrite each other's partials: keep them
+ *     ordered, e.g. on one stream.
+ * The attention pages have no counterpart to this entry point; it exists for
+ * the callers above.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (2u << 20)
+int attn_decode_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int Nq, int Nk, int D, float scale, void* stream);
 
 /* Static description of a status code. */
 const char* attn_strerror(int status);
