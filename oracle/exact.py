@@ -9,7 +9,8 @@ What it computes
 ----------------
 For one attention plane (one (batch, head) pair, or one packed sequence of
 one head) with queries q_i, keys k_j and values v_j, and the allowed key set
-J(i) = {j : j <= i} when causal, else every key:
+J(i) = {j : j <= i + (Nk - Nq)} when causal (j <= i for self-attention),
+else every key:
 
     s_ij   = scale * sum_d q_id k_jd                          (j in J(i))
     m_i    = max_j s_ij
@@ -43,6 +44,14 @@ Sources
   Overview", steps 1-3).  It is used only to check that the tiled form equals
   the materialised one.
 
+Cross-attention (fewer or more query rows than keys) uses the causal
+reading where the queries are the last Nq positions of an Nk-long sequence:
+key j is allowed for query i when j <= i + (Nk - Nq).  The pages mention
+cross-attention (Nq != Nk) without a mask convention ("Python Attention
+Mechanisms Explained", "The Core Idea"); this bottom-right alignment makes a
+cross call on the last Nq queries equal the last Nq rows of self-attention.
+A row with no allowed key has O = 0 and LSE = -inf.
+
 Layouts match the CUDA boundary: dense tensors are (B, H, N, D); packed
 variable-length tensors are (H, N_total, D) with ``cu_seqlens`` of length
 nseq+1, each sequence attending only to itself with positions relative to its
@@ -58,27 +67,42 @@ SLAB_ROWS = 512
 FULL_MATRIX_MAX_N = 4096
 
 
-def _plane_rows(qp, kp, vp, scale, causal, r0, r1):
-    """O and LSE of query rows [r0, r1) of one plane, materialising those score rows."""
+def _plane_rows(qp, kp, vp, scale, causal, r0, r1, offset=0):
+    """O and LSE of query rows [r0, r1) of one plane, materialising those score rows.
+
+    Causal: key j is allowed for query i when j <= i + offset.
+    """
     n_keys = kp.shape[0]
-    kmax = min(n_keys, r1) if causal else n_keys          # keys beyond r1-1 are all masked
+    kmax = max(0, min(n_keys, r1 + offset)) if causal else n_keys   # later keys are masked
+    o = np.zeros((r1 - r0, vp.shape[1]))
+    lse = np.full(r1 - r0, -np.inf)
+    if kmax == 0:
+        return o, lse
     s = scale * (qp[r0:r1] @ kp[:kmax].T)                 # (rows, kmax) fp64
     if causal:
         i = np.arange(r0, r1)[:, None]
         j = np.arange(kmax)[None, :]
-        s = np.where(j <= i, s, -np.inf)
-    m = s.max(axis=1, keepdims=True)
-    e = np.exp(s - m)
+        s = np.where(j <= i + offset, s, -np.inf)
+    live = np.isfinite(s).any(axis=1)                     # rows with at least one allowed key
+    sl = s[live]
+    m = sl.max(axis=1, keepdims=True)
+    e = np.exp(sl - m)
     l = e.sum(axis=1, keepdims=True)
-    o = (e / l) @ vp[:kmax]
-    lse = m[:, 0] + np.log(l[:, 0])
+    o[live] = (e / l) @ vp[:kmax]
+    lse[live] = m[:, 0] + np.log(l[:, 0])
     return o, lse
 
 
-def attention_plane(qp, kp, vp, scale, causal):
-    """Naive materialised attention for one (N, D) plane in fp64."""
+def attention_plane(qp, kp, vp, scale, causal, offset=None):
+    """Naive materialised attention for one plane in fp64.
+
+    qp: (Nq, D), kp: (Nk, D), vp: (Nk, Dv).  The causal offset defaults to
+    Nk - Nq (0 for self-attention).
+    """
     qp, kp, vp = (np.asarray(a, dtype=np.float64) for a in (qp, kp, vp))
     n = qp.shape[0]
+    if offset is None:
+        offset = kp.shape[0] - n
     o = np.empty((n, vp.shape[1]), dtype=np.float64)
     lse = np.empty(n, dtype=np.float64)
     if n == 0:
@@ -86,7 +110,7 @@ def attention_plane(qp, kp, vp, scale, causal):
     step = n if n <= FULL_MATRIX_MAX_N else SLAB_ROWS
     for r0 in range(0, n, step):
         r1 = min(n, r0 + step)
-        o[r0:r1], lse[r0:r1] = _plane_rows(qp, kp, vp, scale, causal, r0, r1)
+        o[r0:r1], lse[r0:r1] = _plane_rows(qp, kp, vp, scale, causal, r0, r1, offset)
     return o, lse
 
 
@@ -124,17 +148,20 @@ def attention(q, k, v, scale, causal, cu_seqlens=None):
     return o, lse
 
 
-def attention_rows(qp, kp, vp, scale, causal, rows):
+def attention_rows(qp, kp, vp, scale, causal, rows, offset=None):
     """O and LSE for selected query rows of one plane (same definition, row by row).
 
     Used to check full-size outputs on a sample of rows.
     """
     qp, kp, vp = (np.asarray(a, dtype=np.float64) for a in (qp, kp, vp))
+    if offset is None:
+        offset = kp.shape[0] - qp.shape[0]
     rows = np.asarray(rows, dtype=np.int64)
     o = np.empty((len(rows), vp.shape[1]), dtype=np.float64)
     lse = np.empty(len(rows), dtype=np.float64)
     for t, r in enumerate(rows):
-        o[t:t + 1], lse[t:t + 1] = _plane_rows(qp, kp, vp, scale, causal, int(r), int(r) + 1)
+        o[t:t + 1], lse[t:t + 1] = _plane_rows(qp, kp, vp, scale, causal, int(r), int(r) + 1,
+                                               offset)
     return o, lse
 
 
@@ -144,7 +171,7 @@ def softmax_probs(qp, kp, scale, causal):
     s = scale * (qp @ kp.T)
     if causal:
         n, nk = s.shape
-        s = np.where(np.arange(nk)[None, :] <= np.arange(n)[:, None], s, -np.inf)
+        s = np.where(np.arange(nk)[None, :] <= np.arange(n)[:, None] + (nk - n), s, -np.inf)
     m = s.max(axis=1, keepdims=True)
     e = np.exp(s - m)
     return e / e.sum(axis=1, keepdims=True)
@@ -162,6 +189,7 @@ def online_tiled(qp, kp, vp, scale, causal, br=128, bc=128):
     """
     qp, kp, vp = (np.asarray(a, dtype=np.float64) for a in (qp, kp, vp))
     n, nk, dv = qp.shape[0], kp.shape[0], vp.shape[1]
+    off = nk - n                                  # causal alignment of the last query to the last key
     o = np.empty((n, dv))
     lse = np.empty(n)
     for i0 in range(0, n, br):
@@ -169,12 +197,13 @@ def online_tiled(qp, kp, vp, scale, causal, br=128, bc=128):
         m = np.full(i1 - i0, -np.inf)
         l = np.zeros(i1 - i0)
         acc = np.zeros((i1 - i0, dv))
-        kend = min(nk, i1) if causal else nk
+        kend = max(0, min(nk, i1 + off)) if causal else nk
         for j0 in range(0, kend, bc):
             j1 = min(kend, j0 + bc)
             s = scale * (qp[i0:i1] @ kp[j0:j1].T)
             if causal:
-                s = np.where(np.arange(j0, j1)[None, :] <= np.arange(i0, i1)[:, None], s, -np.inf)
+                s = np.where(np.arange(j0, j1)[None, :] <= np.arange(i0, i1)[:, None] + off,
+                             s, -np.inf)
             m_new = np.maximum(m, s.max(axis=1))
             # a row whose keys in this tile are all masked and that has seen
             # nothing yet keeps m = -inf; exp(-inf - -inf) would be NaN
@@ -184,6 +213,7 @@ def online_tiled(qp, kp, vp, scale, causal, br=128, bc=128):
             l = alpha * l + p.sum(axis=1)
             acc = alpha[:, None] * acc + p @ vp[j0:j1]
             m = m_new
-        o[i0:i1] = acc / l[:, None]
-        lse[i0:i1] = m + np.log(l)
+        live = l > 0                              # rows that saw no allowed key: O = 0, LSE = -inf
+        o[i0:i1] = np.where(live[:, None], acc / np.where(live, l, 1.0)[:, None], 0.0)
+        lse[i0:i1] = np.where(live, m + np.log(np.where(live, l, 1.0)), -np.inf)
     return o, lse

@@ -348,3 +348,88 @@ def test_key_slices_merge_by_log_sum_exp():
     o_m = sum(np.exp(pl - lse_m)[:, None] * po for po, pl in parts)
     np.testing.assert_allclose(lse_m, lse, rtol=0, atol=1e-12)
     np.testing.assert_allclose(o_m, o, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Causal cross form: Nq != Nk, query i aligned to key i + (Nk - Nq)
+# ---------------------------------------------------------------------------
+
+def _brute_causal_cross(q, k, v, scale):
+    nq, nk = q.shape[0], k.shape[0]
+    o = np.zeros((nq, v.shape[1]))
+    lse = np.full(nq, -np.inf)
+    for i in range(nq):
+        allowed = [j for j in range(nk) if j - (nk - nq) <= i]
+        if not allowed:
+            continue
+        s = {j: scale * math.fsum(q[i, t] * k[j, t] for t in range(q.shape[1])) for j in allowed}
+        mx = max(s.values())
+        e = {j: math.exp(s[j] - mx) for j in allowed}
+        den = math.fsum(e.values())
+        for t in range(v.shape[1]):
+            o[i, t] = math.fsum(e[j] * v[j, t] for j in allowed) / den
+        lse[i] = mx + math.log(den)
+    return o, lse
+
+
+@pytest.mark.parametrize("nq,nk", [(1, 1), (1, 7), (3, 7), (7, 7), (9, 4), (5, 1), (4, 6)])
+def test_causal_cross_brute_force(nq, nk):
+    rng = np.random.default_rng(nq * 17 + nk)
+    q, k, v = _rand(rng, nq, 5), _rand(rng, nk, 5), _rand(rng, nk, 3)
+    o, lse = A.attention_plane(q, k, v, 0.7, True)
+    ro, rl = _brute_causal_cross(q, k, v, 0.7)
+    np.testing.assert_allclose(o, ro, rtol=0, atol=1e-13)
+    assert np.array_equal(np.isinf(lse), np.isinf(rl))
+    fin = np.isfinite(rl)
+    np.testing.assert_allclose(lse[fin], rl[fin], rtol=0, atol=1e-13)
+
+
+def test_causal_cross_is_the_tail_of_self_attention():
+    # With Nq < Nk the queries are the last Nq positions: their output equals
+    # the last Nq rows of causal self-attention over all Nk positions.
+    rng = np.random.default_rng(41)
+    n, d = 300, 16
+    q, k, v = _rand(rng, n, d), _rand(rng, n, d), _rand(rng, n, d)
+    o, lse = A.attention_plane(q, k, v, 0.25, True)
+    for nq in (1, 2, 129, 299):
+        oc, lc = A.attention_plane(q[n - nq:], k, v, 0.25, True)
+        # same arithmetic up to the BLAS blocking of a different row count
+        np.testing.assert_allclose(oc, o[n - nq:], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lc, lse[n - nq:], rtol=0, atol=1e-13)
+
+
+def test_causal_cross_more_queries_than_keys():
+    # With Nq > Nk the first Nq - Nk queries see no key (O = 0, LSE = -inf)
+    # and query Nq - Nk + t sees keys 0..t: its output is V[0] when t = 0.
+    rng = np.random.default_rng(42)
+    q, k, v = _rand(rng, 10, 8), _rand(rng, 4, 8), _rand(rng, 4, 8)
+    o, lse = A.attention_plane(q, k, v, 0.5, True)
+    assert (o[:6] == 0).all() and np.isneginf(lse[:6]).all()
+    np.testing.assert_array_equal(o[6], v[0])
+    assert lse[6] == pytest.approx(0.5 * float(q[6] @ k[0]), abs=1e-14)
+    # the last query sees every key: the non-causal result for that row
+    on, ln_ = A.attention_plane(q[9:], k, v, 0.5, False)
+    np.testing.assert_allclose(o[9], on[0], rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("nq,nk", [(1, 300), (77, 300), (300, 77), (200, 200), (130, 1)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_online_tiled_cross_equals_materialised(nq, nk, causal):
+    rng = np.random.default_rng(nq + 3 * nk)
+    q, k, v = _rand(rng, nq, 8), _rand(rng, nk, 8), _rand(rng, nk, 8)
+    o, lse = A.attention_plane(q, k, v, 0.35, causal)
+    ot, lt = A.online_tiled(q, k, v, 0.35, causal, br=64, bc=32)
+    np.testing.assert_allclose(ot, o, rtol=0, atol=1e-12)
+    assert np.array_equal(np.isneginf(lt), np.isneginf(lse))
+    fin = np.isfinite(lse)
+    np.testing.assert_allclose(lt[fin], lse[fin], rtol=0, atol=1e-12)
+
+
+def test_cross_rows_equal_plane():
+    rng = np.random.default_rng(43)
+    q, k, v = _rand(rng, 50, 8), _rand(rng, 180, 8), _rand(rng, 180, 8)
+    o, lse = A.attention_plane(q, k, v, 0.3, True)
+    rows = [0, 1, 17, 49]
+    ro, rl = A.attention_rows(q, k, v, 0.3, True, rows)
+    np.testing.assert_allclose(ro, o[rows], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(rl, lse[rows], rtol=0, atol=1e-13)
