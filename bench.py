@@ -219,7 +219,8 @@ def oracle_rows_sample(w, x, plane_index: int, rows: np.ndarray, threads: int):
         with ThreadPoolExecutor(max_workers=threads) as ex:
             list(ex.map(lambda r: oracle.attention_rows(q, k, v, w.scale, w.causal, r), chunks))
         dt = time.perf_counter() - t0
-    keys = (rows + 1) if w.causal else np.full(len(rows), w.N)
+    nk = w.n_keys
+    keys = np.clip(rows + 1 + (nk - w.N), 0, nk) if w.causal else np.full(len(rows), nk)
     flops = float(4.0 * w.D * keys.sum())
     return flops, dt
 
@@ -279,6 +280,9 @@ def workload_config(w):
            "dtype_in": w.dtype, "flops_per_step": w.flops(),
            "l2": "inputs larger than L2 (no flush)" if 3 * w.hbm_bytes() / 4 > 126e6
            else "L2 flushed between steps"}
+    if w.is_cross:
+        cfg["Nk"] = w.n_keys
+        cfg["mask_alignment"] = "bottom-right (key j allowed for query i when j <= i + Nk - N)"
     if w.varlen is not None:
         cfg["seq_lens"] = list(w.varlen)
     return cfg
@@ -302,6 +306,7 @@ def run_ours(args, w):
     dev = torch.device("cuda", local)
     q, k, v = (t.to(dev) for t in (x["q"], x["k"], x["v"]))
     cu = None if x["cu_seqlens"] is None else torch.as_tensor(x["cu_seqlens"]).to(dev)
+    cuk = None if x["cu_seqlens_k"] is None else torch.as_tensor(x["cu_seqlens_k"]).to(dev)
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -313,7 +318,7 @@ def run_ours(args, w):
         if flush is not None:
             flush.zero_()
         attention_forward(q, k, v, causal=w.causal, scale=w.scale, cu_seqlens=cu, out=o, lse=lse,
-                          stream=stream)
+                          stream=stream, cu_seqlens_k=cuk)
 
     for _ in range(args.warmup):
         step()
@@ -335,7 +340,7 @@ def run_ours(args, w):
                 flush.zero_()
             starts[i].record(stream)
             attention_forward(q, k, v, causal=w.causal, scale=w.scale, cu_seqlens=cu, out=o,
-                              lse=lse, stream=stream)
+                              lse=lse, stream=stream, cu_seqlens_k=cuk)
             ends[i].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
@@ -368,7 +373,7 @@ def run_ours(args, w):
         k.copy_(hk, non_blocking=True)
         v.copy_(hv, non_blocking=True)
         attention_forward(q, k, v, causal=w.causal, scale=w.scale, cu_seqlens=cu, out=o, lse=lse,
-                          stream=stream)
+                          stream=stream, cu_seqlens_k=cuk)
         ho.copy_(o, non_blocking=True)
         hl.copy_(lse, non_blocking=True)
     e1.record(stream)
@@ -474,23 +479,32 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default=W.HEADLINE,
+                    choices=sorted(W.WORKLOADS) + sorted(W.CROSS_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", choices=["forward", "decode"], default="forward",
                     help="decode: the KV-cache decode path (GB/s against HBM)")
     ap.add_argument("--decode-shape", default="8,32,1,32768,128", help="B,H,Nq,Nk,D for --op decode")
     ap.add_argument("--shape", default=None,
-                    help="B,H,N,D: same dtype and mask as --workload at another size "
-                         "(profiling cases)")
+                    help="B,H,N,D (or B,H,Nq,Nk,D for cross-attention): same dtype and mask "
+                         "as --workload at another size (profiling cases)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     if args.op == "decode":
         return run_decode(args)
-    w = W.WORKLOADS[args.workload]
+    w = {**W.WORKLOADS, **W.CROSS_WORKLOADS}[args.workload]
     if args.shape:
-        b, h, n, d = (int(t) for t in args.shape.split(","))
+        dims = [int(t) for t in args.shape.split(",")]
+        if len(dims) == 4:
+            b, h, n, d = dims
+            nk = None
+            tag = f"n{n}"
+        else:
+            b, h, n, nk, d = dims
+            tag = f"nq{n}_nk{nk}"
         w = W.custom(w.dtype, B=b, H=h, N=n, D=d, causal=w.causal, seed=w.seed, qk_std=w.qk_std,
-                     name=f"{w.dtype}_{'causal_' if w.causal else ''}b{b}_h{h}_n{n}_d{d}")
+                     Nk=nk, name=f"{w.dtype}_{'cross_' if nk is not None else ''}"
+                                 f"{'causal_' if w.causal else ''}b{b}_h{h}_{tag}_d{d}")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

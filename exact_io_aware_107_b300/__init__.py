@@ -30,35 +30,54 @@ def _ptr(t):
 
 
 def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens=None, out=None, lse=None,
-                      stream=None):
+                      stream=None, cu_seqlens_k=None):
     """O and LSE of softmax(scale * Q K^T + causal mask) V.
 
     q, k, v: CUDA tensors, bf16 or fp16 (D in {64, 128}) or fp32 (D <= 128), contiguous,
     (B, H, N, D), or (H, N_total, D) with ``cu_seqlens`` (int32 CUDA tensor of
     nseq+1 offsets).  Returns (O, LSE) with O like q and LSE fp32 (B, H, N) or
     (H, N_total).  Enqueued on ``stream`` (default: torch's current stream).
+
+    Cross-attention: k and v may have a different sequence length Nk than q
+    (dense), or their own offsets ``cu_seqlens_k`` (packed).  The causal mask
+    then allows key j for query i when j <= i + (Nk - Nq) (the last query sees
+    every key); a query with no allowed key gets O = 0 and LSE = -inf.
     """
     import torch
 
     if q.dtype != k.dtype or q.dtype != v.dtype:
         raise TypeError("q, k, v must share a dtype")
-    if q.shape != k.shape or q.shape != v.shape:
-        raise ValueError("q, k, v must share a shape")
+    if k.shape != v.shape:
+        raise ValueError("k and v must share a shape")
     for t in (q, k, v):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("q, k, v must be contiguous CUDA tensors")
-    if cu_seqlens is None:
-        if q.dim() != 4:
+    cus = []
+    for c in (cu_seqlens, cu_seqlens_k):
+        if c is not None and (c.dtype != torch.int32 or not c.is_cuda or c.dim() != 1):
+            raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+        cus.append(None if c is None else c.contiguous())
+    cu_q, cu_k = cus
+    if cu_q is None:
+        if cu_k is not None:
+            raise ValueError("cu_seqlens_k needs cu_seqlens")
+        if q.dim() != 4 or k.dim() != 4:
             raise ValueError("dense layout is (B, H, N, D)")
         B, H, N, D = q.shape
+        Nk = k.shape[2]
+        if k.shape != (B, H, Nk, D):
+            raise ValueError("k, v must be (B, H, Nk, D) with q's B, H, D")
     else:
-        if q.dim() != 3:
+        if q.dim() != 3 or k.dim() != 3:
             raise ValueError("packed layout is (H, N_total, D)")
-        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
-            raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
         H, N, D = q.shape
-        B = cu_seqlens.numel() - 1
-        cu_seqlens = cu_seqlens.contiguous()
+        B = cu_q.numel() - 1
+        Nk = k.shape[1]
+        if k.shape != (H, Nk, D):
+            raise ValueError("k, v must be (H, Nk_total, D) with q's H, D")
+        if cu_k is not None and cu_k.numel() != cu_q.numel():
+            raise ValueError("cu_seqlens and cu_seqlens_k must have the same length")
+    cross = Nk != N or cu_k is not None
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
@@ -68,19 +87,24 @@ def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens=None, out=No
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     handle = stream.cuda_stream
-    if q.dtype == torch.bfloat16:
-        rc = _binding.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, D,
-                               _ptr(cu_seqlens), causal, scale, handle)
-    elif q.dtype == torch.float16:
-        rc = _binding.attn_fwd_f16(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, D,
-                                   _ptr(cu_seqlens), causal, scale, handle)
-    elif q.dtype == torch.float32:
-        rc = _binding.attn_fwd_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, D,
-                                   _ptr(cu_seqlens), causal, scale, handle)
-    else:
+    kinds = {torch.bfloat16: (_binding.attn_fwd, _binding.ATTN_BF16),
+             torch.float16: (_binding.attn_fwd_f16, _binding.ATTN_F16),
+             torch.float32: (_binding.attn_fwd_f32, _binding.ATTN_F32)}
+    if q.dtype not in kinds:
         raise TypeError("dtype must be bfloat16, float16 or float32")
+    fn, dtype = kinds[q.dtype]
+    if cross:
+        if cu_q is not None and cu_k is None:
+            cu_k = cu_q
+        rc = _binding.attn_fwd_cross(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, Nk,
+                                     D, _ptr(cu_q), _ptr(cu_k), causal, scale, dtype, handle)
+        where = "attention_forward (cross)"
+    else:
+        rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, D, _ptr(cu_q), causal,
+                scale, handle)
+        where = "attention_forward"
     if rc != _binding.ATTN_OK:
-        raise AttnError(rc, "attention_forward")
+        raise AttnError(rc, where)
     return out, lse
 
 

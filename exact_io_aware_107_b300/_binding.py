@@ -28,6 +28,10 @@ ATTN_ERR_TIMEOUT = -7
 ATTN_ERR_BOUNDS = -8
 ATTN_ERR_SCALE = -9
 ATTN_ERR_SCRATCH = -10
+ATTN_ERR_DTYPE = -11
+ATTN_BF16 = 0
+ATTN_F16 = 1
+ATTN_F32 = 2
 NOALLOC_SCRATCH_BYTES = 2 << 20
 
 # Every symbol include/attn_b300.h declares, with its ctypes signature.
@@ -38,6 +42,9 @@ _SIGNATURES = {
                      + [ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p]),
     "attn_fwd_f32": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4
                      + [ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p]),
+    "attn_fwd_cross": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
+                       + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
+                          ctypes.c_int, ctypes.c_void_p]),
     "attn_decode": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
                     + [ctypes.c_float, ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_void_p]),
     "attn_decode_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
@@ -99,6 +106,14 @@ def attn_fwd_f32(q, k, v, o, lse, B, H, N, D, cu_seqlens, causal, scale, stream)
     """fp32 forward; pointers are ints (device addresses) or None."""
     return load().attn_fwd_f32(q, k, v, o, lse, int(B), int(H), int(N), int(D), cu_seqlens,
                                int(causal), float(scale), stream)
+
+
+def attn_fwd_cross(q, k, v, o, lse, B, H, Nq, Nk, D, cu_seqlens_q, cu_seqlens_k, causal, scale,
+                   dtype, stream) -> int:
+    """Forward with Nq queries and Nk keys (ATTN_BF16 / ATTN_F16 / ATTN_F32)."""
+    return load().attn_fwd_cross(q, k, v, o, lse, int(B), int(H), int(Nq), int(Nk), int(D),
+                                 cu_seqlens_q, cu_seqlens_k, int(causal), float(scale),
+                                 int(dtype), stream)
 
 
 def attn_decode(q, k, v, o, lse, B, H, Nq, Nk, D, scale, workspace, workspace_bytes,

@@ -150,22 +150,23 @@ int prepare_device(DeviceState** out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Shared argument checks of both entry points.
+// Argument checks shared by every forward entry point.  Nk == 0 is allowed
+// (every query then sees no key), and k, v may be NULL in that case.
 int check_common(const void* q, const void* k, const void* v, const void* o, const void* lse,
-                 int B, int H, int N, int D, const int* cu_seqlens, float scale) {
-  if (B < 1 || H < 1 || N < 0) return ATTN_ERR_SHAPE;
+                 int B, int H, int Nq, int Nk, const int* cu_q, const int* cu_k, float scale) {
+  if (B < 1 || H < 1 || Nq < 0 || Nk < 0) return ATTN_ERR_SHAPE;
+  if ((cu_q == nullptr) != (cu_k == nullptr)) return ATTN_ERR_NULL;
   if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_SCALE;
-  if (N == 0) return ATTN_OK;
-  if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
+  if (Nq == 0) return ATTN_OK;
+  if (!q || !o || !lse || (Nk > 0 && (!k || !v))) return ATTN_ERR_NULL;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       !aligned(lse, 4))
     return ATTN_ERR_ALIGN;
-  if (cu_seqlens && !aligned(cu_seqlens, 4)) return ATTN_ERR_ALIGN;
+  if ((cu_q && !aligned(cu_q, 4)) || (cu_k && !aligned(cu_k, 4))) return ATTN_ERR_ALIGN;
   // element counts must fit the 64-bit offsets and the int row indices
-  const long long planes = cu_seqlens ? static_cast<long long>(H) : 1LL * B * H;
+  const long long planes = cu_q ? static_cast<long long>(H) : 1LL * B * H;
   if (planes > (1LL << 31) - 1) return ATTN_ERR_SHAPE;
-  if (planes * N > (1LL << 40)) return ATTN_ERR_SHAPE;
-  (void)D;
+  if (planes * Nq > (1LL << 40) || planes * Nk > (1LL << 40)) return ATTN_ERR_SHAPE;
   return ATTN_OK;
 }
 
@@ -201,37 +202,42 @@ __global__ void wait_selftest_kernel(unsigned long long budget, unsigned int* er
 
 
 
-// Shared body of the two 16-bit entry points (bf16 and fp16).
+// 16-bit (bf16 or fp16) forward on the tcgen05 kernel.
 int fwd_16bit(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-              int N, int D, const int* cu_seqlens, int causal, float scale, void* stream,
-              bool f16) {
-  int rc = check_common(q, k, v, o, lse, B, H, N, D, cu_seqlens, scale);
-  if (rc != ATTN_OK) return rc;
+              int Nq, int Nk, int D, const int* cu_q, const int* cu_k, int causal, float scale,
+              cudaStream_t s, bool f16) {
   if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
-  if (N == 0) return ATTN_OK;
+  if (Nq == 0) return ATTN_OK;
   DeviceState* st = nullptr;
-  rc = prepare_device(&st);
+  int rc = prepare_device(&st);
   if (rc != ATTN_OK) return rc;
 
-  const int planes = cu_seqlens ? H : B * H;
+  const int planes = cu_q ? H : B * H;
   CUtensorMap mq, mk, mv;
-  if (encode_16bit_map(&mq, q, D, N, planes, f16) != ATTN_OK ||
-      encode_16bit_map(&mk, k, D, N, planes, f16) != ATTN_OK ||
-      encode_16bit_map(&mv, v, D, N, planes, f16) != ATTN_OK)
-    return ATTN_ERR_LAUNCH;
+  if (encode_16bit_map(&mq, q, D, Nq, planes, f16) != ATTN_OK) return ATTN_ERR_LAUNCH;
+  if (Nk > 0) {
+    if (encode_16bit_map(&mk, k, D, Nk, planes, f16) != ATTN_OK ||
+        encode_16bit_map(&mv, v, D, Nk, planes, f16) != ATTN_OK)
+      return ATTN_ERR_LAUNCH;
+  } else {
+    mk = mq;  // no key: the kernel issues no K/V load
+    mv = mq;
+  }
 
   Bf16Params p;
   p.o = o;
   p.lse = lse;
-  p.cu_seqlens = cu_seqlens;
-  p.nseq = cu_seqlens ? B : 0;
+  p.cu_seqlens = cu_q;
+  p.cu_seqlens_k = cu_k;
+  p.nseq = cu_q ? B : 0;
   p.planes = planes;
-  p.rows = N;
-  p.n_qblk = (N + 255) / 256;
+  p.rows = Nq;
+  p.rows_k = Nk;
+  p.n_qblk = (Nq + 255) / 256;
   // work items: packed -> single 256-row blocks (an upper bound, surplus
   // entries are skipped); dense -> pairs of mirror blocks of one plane
-  const long long tiles = cu_seqlens ? (1LL * (N / 256 + B) * H) : (1LL * p.n_qblk * planes);
-  const long long items = cu_seqlens ? tiles : 1LL * ((p.n_qblk + 1) / 2) * planes;
+  const long long tiles = cu_q ? (1LL * (Nq / 256 + B) * H) : (1LL * p.n_qblk * planes);
+  const long long items = cu_q ? tiles : 1LL * ((p.n_qblk + 1) / 2) * planes;
   if (tiles > 0x7fffffffLL) return ATTN_ERR_SHAPE;
   p.n_tiles = static_cast<int>(tiles);
   p.causal = causal ? 1 : 0;
@@ -240,7 +246,6 @@ int fwd_16bit(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.err = st->err;
 
   const unsigned grid = static_cast<unsigned>(std::min<long long>(items, st->sms));
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (D == 64) {
     if (f16)
       attn_fwd_bf16_kernel<64, true><<<grid, Bf16Cfg<64>::THREADS, Bf16Cfg<64>::SMEM_ALLOC, s>>>(
@@ -257,6 +262,58 @@ int fwd_16bit(const void* q, const void* k, const void* v, void* o, float* lse, 
                                          s>>>(mq, mk, mv, p);
   }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+// fp32 forward on CUDA cores.
+int fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int H,
+            int Nq, int Nk, int D, const int* cu_q, const int* cu_k, int causal, float scale,
+            cudaStream_t s) {
+  if (D < 1 || D > 128) return ATTN_ERR_HEADDIM;
+  if (Nq == 0) return ATTN_OK;
+  DeviceState* st = nullptr;
+  const int rc = prepare_device(&st);
+  if (rc != ATTN_OK) return rc;
+
+  F32Params p;
+  p.o = o;
+  p.lse = lse;
+  p.cu_seqlens = cu_q;
+  p.cu_seqlens_k = cu_k;
+  p.nseq = cu_q ? B : 0;
+  p.planes = cu_q ? H : B * H;
+  p.rows = Nq;
+  p.rows_k = Nk;
+  p.n_qblk = cu_q ? (Nq / kF32BM + B) : (Nq + kF32BM - 1) / kF32BM;
+  p.D = D;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.err = st->err;
+  const long long grid = 1LL * p.n_qblk * p.planes;
+  if (grid > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  const int smem = (2 * kF32BM * D + kF32BN * (D + 1)) * 4;
+  attn_fwd_f32_kernel<4><<<static_cast<unsigned>(grid), 128, smem, s>>>(q, k, v, p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+// Every forward entry point ends here.
+int fwd_any(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+            int Nq, int Nk, int D, const int* cu_q, const int* cu_k, int causal, float scale,
+            int dtype, void* stream) {
+  const int rc = check_common(q, k, v, o, lse, B, H, Nq, Nk, cu_q, cu_k, scale);
+  if (rc != ATTN_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  switch (dtype) {
+    case ATTN_BF16:
+    case ATTN_F16:
+      return fwd_16bit(q, k, v, o, lse, B, H, Nq, Nk, D, cu_q, cu_k, causal, scale, s,
+                       dtype == ATTN_F16);
+    case ATTN_F32:
+      return fwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                     static_cast<const float*>(v), static_cast<float*>(o), lse, B, H, Nq, Nk, D,
+                     cu_q, cu_k, causal, scale, s);
+    default:
+      return ATTN_ERR_DTYPE;
+  }
 }
 
 // Key slices per plane for the decode kernel: enough CTAs to cover every SM
@@ -421,44 +478,30 @@ extern "C" int attn_decode(const void* q, const void* k, const void* v, void* o,
 extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int H, int N, int D, const int* cu_seqlens, int causal, float scale,
                         void* stream) {
-  return attn::fwd_16bit(q, k, v, o, lse, B, H, N, D, cu_seqlens, causal, scale, stream, false);
+  return fwd_any(q, k, v, o, lse, B, H, N, N, D, cu_seqlens, cu_seqlens, causal, scale, ATTN_BF16,
+                 stream);
 }
 
 extern "C" int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int H, int N, int D, const int* cu_seqlens, int causal,
                             float scale, void* stream) {
-  return attn::fwd_16bit(q, k, v, o, lse, B, H, N, D, cu_seqlens, causal, scale, stream, true);
+  return fwd_any(q, k, v, o, lse, B, H, N, N, D, cu_seqlens, cu_seqlens, causal, scale, ATTN_F16,
+                 stream);
 }
 
 extern "C" int attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
                             int B, int H, int N, int D, const int* cu_seqlens, int causal,
                             float scale, void* stream) {
-  int rc = check_common(q, k, v, o, lse, B, H, N, D, cu_seqlens, scale);
-  if (rc != ATTN_OK) return rc;
-  if (D < 1 || D > 128) return ATTN_ERR_HEADDIM;
-  if (N == 0) return ATTN_OK;
-  DeviceState* st = nullptr;
-  rc = prepare_device(&st);
-  if (rc != ATTN_OK) return rc;
+  return fwd_any(q, k, v, o, lse, B, H, N, N, D, cu_seqlens, cu_seqlens, causal, scale, ATTN_F32,
+                 stream);
+}
 
-  F32Params p;
-  p.o = o;
-  p.lse = lse;
-  p.cu_seqlens = cu_seqlens;
-  p.nseq = cu_seqlens ? B : 0;
-  p.planes = cu_seqlens ? H : B * H;
-  p.rows = N;
-  p.n_qblk = cu_seqlens ? (N / kF32BM + B) : (N + kF32BM - 1) / kF32BM;
-  p.D = D;
-  p.causal = causal ? 1 : 0;
-  p.scale = scale;
-  p.err = st->err;
-  const long long grid = 1LL * p.n_qblk * p.planes;
-  if (grid > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-  const int smem = (2 * kF32BM * D + kF32BN * (D + 1)) * 4;
-  attn_fwd_f32_kernel<4><<<static_cast<unsigned>(grid), 128, smem,
-                           static_cast<cudaStream_t>(stream)>>>(q, k, v, p);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+extern "C" int attn_fwd_cross(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H, int Nq, int Nk, int D, const int* cu_seqlens_q,
+                              const int* cu_seqlens_k, int causal, float scale, int dtype,
+                              void* stream) {
+  return fwd_any(q, k, v, o, lse, B, H, Nq, Nk, D, cu_seqlens_q, cu_seqlens_k, causal, scale,
+                 dtype, stream);
 }
 
 extern "C" const char* attn_strerror(int status) {
@@ -475,6 +518,7 @@ extern "C" const char* attn_strerror(int status) {
     case ATTN_ERR_SCALE: return "scale must be finite and > 0";
     case ATTN_ERR_SCRATCH:
       return "decode partials need more than the built-in scratch (ATTN_NOALLOC_SCRATCH_BYTES)";
+    case ATTN_ERR_DTYPE: return "element type not one of ATTN_BF16, ATTN_F16, ATTN_F32";
     default: return "unknown status";
   }
 }
@@ -513,4 +557,4 @@ extern "C" int attn_wait_selftest(unsigned long long timeout_ns, void* stream) {
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
-extern "C" int attn_version(void) { return 100; }
+extern "C" int attn_version(void) { return 200; }

@@ -16,6 +16,12 @@
 // Attention Mechanisms Explained", section "Causal Masking and Incremental
 // Decoding").
 //
+// Queries and keys may differ in length (cross-attention, named in the same
+// page's section "The Core Idea").  The causal mask then aligns the last query
+// with the last key: key j is allowed for query i when j <= i + (Nk - Nq),
+// which is j <= i when Nq == Nk.  A query with no allowed key (i < Nq - Nk)
+// gets O = 0 and LSE = -inf.
+//
 // CTA layout (320 threads, one persistent CTA per SM):
 //   warps 0-3  softmax and epilogue for query tile 0 (thread t owns row t =
 //              TMEM lane t)
@@ -52,13 +58,15 @@
 namespace attn {
 
 struct Bf16Params {
-  void* o;                // bf16 or fp16 output, same layout as q
+  void* o;                  // bf16 or fp16 output, same layout as q
   float* lse;
-  const int* cu_seqlens;  // nullptr for the dense layout
-  int nseq;               // packed layout: number of sequences
-  int planes;             // dense: B*H; packed: H
-  int rows;               // dense: N; packed: total tokens
-  int n_qblk;             // dense: ceil(N/256)
+  const int* cu_seqlens;    // query offsets; nullptr for the dense layout
+  const int* cu_seqlens_k;  // key offsets (packed layout only)
+  int nseq;                 // packed layout: number of sequences
+  int planes;               // dense: B*H; packed: H
+  int rows;                 // query rows per plane (dense: Nq; packed: total query tokens)
+  int rows_k;               // key rows per plane (dense: Nk; packed: total key tokens)
+  int n_qblk;               // dense: ceil(Nq/256)
   int n_tiles;            // packed: an upper bound on the work tiles
   int causal;
   float scale_log2;       // scale * log2(e)
@@ -94,10 +102,13 @@ struct Bf16Cfg {
 // One work tile: 256 query rows of one plane / sequence.
 struct WorkTile {
   int plane;     // tensor-map plane coordinate (dense: b*H+h; packed: h)
-  int row_base;  // first row of the sequence in the tensor map (0 when dense)
-  int seq_len;   // keys (and query rows) of the sequence
+  int row_base;  // first query row of the sequence in the query map (0 when dense)
+  int seq_len;   // query rows of the sequence
+  int kv_base;   // first key row of the sequence in the key/value maps
+  int kv_len;    // keys of the sequence
   int qblk;      // 256-row block index within the sequence
-  int n0, n1;    // key tiles visited by query tile 0 and 1 (0: tile absent)
+  bool has_q1;   // the block has a second 128-row query tile
+  int n0, n1;    // key tiles visited by query tile 0 and 1 (0: none, or tile absent)
 };
 
 // Cursor over packed sequences; every CTA's list positions increase, so the
@@ -123,6 +134,8 @@ enum TileStep { kTileEnd = 0, kTileRun = 1, kTileSkip = 2 };
 //
 // Returns kTileEnd past the last tile (or when cu_seqlens is malformed),
 // kTileSkip for the empty second half of a pair whose two blocks coincide.
+// A query tile whose rows see no key at all has n_i == 0: no loads and no
+// MMAs, its softmax warps write O = 0 and LSE = -inf directly.
 __device__ __forceinline__ int bf16_tile(const Bf16Params& p, int it, SeqCursor& cur,
                                          WorkTile& w) {
   const int grid = static_cast<int>(gridDim.x);
@@ -143,6 +156,8 @@ __device__ __forceinline__ int bf16_tile(const Bf16Params& p, int it, SeqCursor&
     }
     w.row_base = 0;
     w.seq_len = p.rows;
+    w.kv_base = 0;
+    w.kv_len = p.rows_k;
   } else {
     const int u = it * grid + ((it & 1) ? grid - 1 - c : c);
     if (u >= p.n_tiles) return kTileEnd;
@@ -157,8 +172,15 @@ __device__ __forceinline__ int bf16_tile(const Bf16Params& p, int it, SeqCursor&
       }
       const int nb = (e - a + 255) / 256;
       if (vb < cur.cum + nb) {
+        const int ak = __ldg(p.cu_seqlens_k + cur.s), ek = __ldg(p.cu_seqlens_k + cur.s + 1);
+        if (ak < 0 || ek < ak || ek > p.rows_k) {
+          if (threadIdx.x == 0) atomicOr(p.err, kDevErrBounds);
+          return kTileEnd;
+        }
         w.row_base = a;
         w.seq_len = e - a;
+        w.kv_base = ak;
+        w.kv_len = ek - ak;
         w.qblk = nb - 1 - (vb - cur.cum);
         found = true;
         break;
@@ -168,10 +190,17 @@ __device__ __forceinline__ int bf16_tile(const Bf16Params& p, int it, SeqCursor&
     }
     if (!found) return kTileEnd;
   }
-  const int nkv = (w.seq_len + 127) / 128;
-  const bool has_q1 = w.qblk * 256 + 128 < w.seq_len;
-  w.n0 = p.causal ? min(nkv, 2 * w.qblk + 1) : nkv;
-  w.n1 = has_q1 ? (p.causal ? min(nkv, 2 * w.qblk + 2) : nkv) : 0;
+  const int nkv = (w.kv_len + 127) / 128;
+  // causal: the last key any row of the query tile at q0 may see
+  const int off = w.kv_len - w.seq_len;
+  auto visited = [&](int q0) {
+    if (!p.causal) return nkv;
+    const int last = min(q0 + 127, w.seq_len - 1) + off;
+    return last < 0 ? 0 : min(nkv, last / 128 + 1);
+  };
+  w.has_q1 = w.qblk * 256 + 128 < w.seq_len;
+  w.n0 = visited(w.qblk * 256);
+  w.n1 = w.has_q1 ? visited(w.qblk * 256 + 128) : 0;
   return kTileRun;
 }
 
@@ -277,10 +306,22 @@ __global__ void __launch_bounds__(320, 1)
     for (int it = 0;; ++it) {
       const int step = bf16_tile(p, it, cur, w);
       if (step == kTileEnd) break;
+      if (step == kTileSkip || (ti == 1 && !w.has_q1)) continue;
       const int n_i = ti ? w.n1 : w.n0;
-      if (step == kTileSkip || n_i == 0) continue;
       const int q_first = w.qblk * 256 + 128 * ti;  // first row of this query tile
       const int row = q_first + t;
+      const int off = w.kv_len - w.seq_len;         // causal alignment of queries to keys
+      if (n_i == 0) {
+        // every row of this tile sees no key
+        if (row < w.seq_len) {
+          const size_t grow = static_cast<size_t>(w.plane) * p.rows + w.row_base + row;
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + grow * D);
+#pragma unroll
+          for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+          p.lse[grow] = -INFINITY;
+        }
+        continue;
+      }
       float m_ref = -INFINITY;
       float l = 0.f;
       bool ok = true;
@@ -296,9 +337,9 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld128_wait(tS, sr);
         const int kv0 = j * C::BN;
         const bool need_mask =
-            (kv0 + C::BN > w.seq_len) || (p.causal && kv0 + C::BN - 1 > q_first);
+            (kv0 + C::BN > w.kv_len) || (p.causal && kv0 + C::BN - 1 > q_first + off);
         if (need_mask) {
-          const int lim = p.causal ? min(w.seq_len - 1, row) : (w.seq_len - 1);
+          const int lim = p.causal ? min(w.kv_len - 1, row + off) : (w.kv_len - 1);
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (kv0 + c > lim) sr[c] = __float_as_uint(-INFINITY);
@@ -367,7 +408,8 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const bool valid = row < w.seq_len;
       const size_t grow = static_cast<size_t>(w.plane) * p.rows + w.row_base + row;
-      const float inv_l = 1.f / l;
+      // l == 0 only for a row that saw no allowed key: O = 0, LSE = -inf
+      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + grow * D);
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
@@ -384,7 +426,7 @@ __global__ void __launch_bounds__(320, 1)
             dst[cc * 4 + v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
         }
       }
-      if (valid) p.lse[grow] = (m_ref + log2f(l)) * 0.69314718055994530942f;
+      if (valid) p.lse[grow] = (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
@@ -408,6 +450,7 @@ __global__ void __launch_bounds__(320, 1)
       if (step == kTileEnd) break;
       if (step == kTileSkip) continue;
       const int nmax = max(w.n0, w.n1);
+      if (nmax == 0) continue;  // no key for either query tile
       if (!wait(&kv_full[g % NS], (g / NS) & 1)) {
         ok = false;
         break;
@@ -493,7 +536,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
       for (int c = 0; c < C::NCHUNK; ++c)
         tma_load_3d_warp(kv_smem + s * C::TILE_BYTES + c * C::CHUNK_BYTES, (t & 1) ? &tmV : &tmK,
-                         smem_u32(&kv_full[s]), c * 64, w.row_base + (t >> 1) * C::BN, w.plane);
+                         smem_u32(&kv_full[s]), c * 64, w.kv_base + (t >> 1) * C::BN, w.plane);
       ++g;
       return true;
     };

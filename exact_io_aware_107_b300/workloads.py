@@ -23,6 +23,9 @@ Recipes
   to bfloat16 with round-to-nearest-even.
 * ``bf16_varlen_causal``: ``default_rng(7)``; 16 lengths from
   ``integers(256, 8193)``, then Q, K, V of shape (H, sum(lengths), D).
+* Cross-attention workloads (``Nk`` set, keys of another length than the
+  queries): the same ``default_rng`` draw order Q, K, V, with K and V of
+  shape (B, H, Nk, D), or (H, sum(varlen_k), D) when packed.
 """
 
 from __future__ import annotations
@@ -48,6 +51,16 @@ class Workload:
     generator: str = "default_rng"   # or "legacy"
     varlen: Optional[tuple] = None   # sequence lengths for the packed layout
     len_draw: Optional[tuple] = None  # (nseq, lo, hi) when the lengths came from the same generator
+    Nk: Optional[int] = None         # keys per plane (total keys for varlen); None: Nk == N
+    varlen_k: Optional[tuple] = None  # key lengths per sequence (packed cross-attention)
+
+    @property
+    def n_keys(self) -> int:
+        return self.N if self.Nk is None else self.Nk
+
+    @property
+    def is_cross(self) -> bool:
+        return self.Nk is not None
 
     @property
     def scale(self) -> float:
@@ -55,23 +68,30 @@ class Workload:
         return float(np.float32(1.0 / math.sqrt(self.D)))
 
     def flops(self) -> float:
-        """Attention-forward FLOPs: 4*N^2*D per (b,h), halved when causal.
+        """Attention-forward FLOPs: 4*D per (query, key) pair, N^2 pairs per (b,h),
+        halved when causal.
 
         For varlen the sum runs over sequences.  The causal halving is the
-        usual convention (it counts N^2/2 pairs, not N(N+1)/2).
+        usual convention (it counts N^2/2 pairs, not N(N+1)/2).  With Nq
+        queries and Nk keys the pairs are Nq*Nk, and under the causal mask
+        (last query aligned with the last key) Nq*Nk - Nq^2/2 when Nq <= Nk,
+        else Nk^2/2: the same convention, which gives N^2/2 at Nq == Nk.
         """
+        def pairs(nq, nk):
+            if not self.causal:
+                return float(nq) * nk
+            return float(nq) * nk - nq * nq / 2.0 if nq <= nk else nk * nk / 2.0
         if self.varlen is not None:
-            pairs = sum(L * L for L in self.varlen)
-            f = 4.0 * self.H * pairs * self.D
-        else:
-            f = 4.0 * self.B * self.H * self.N * self.N * self.D
-        return f / 2 if self.causal else f
+            lk = self.varlen_k if self.varlen_k is not None else self.varlen
+            return 4.0 * self.H * self.D * sum(pairs(a, b) for a, b in zip(self.varlen, lk))
+        return 4.0 * self.B * self.H * self.D * pairs(self.N, self.n_keys)
 
     def hbm_bytes(self) -> float:
         """Algorithmic HBM bytes: Q, K, V read once, O and LSE written once."""
         elt = 4 if self.dtype == "f32" else 2
-        rows = self.H * self.N if self.varlen is not None else self.B * self.H * self.N
-        return 4.0 * rows * self.D * elt + rows * 4.0
+        planes = self.H if self.varlen is not None else self.B * self.H
+        rows, keys = planes * self.N, planes * self.n_keys
+        return (2.0 * rows + 2.0 * keys) * self.D * elt + rows * 4.0
 
 
 def _varlen_lengths(seed: int, nseq: int, lo: int, hi: int) -> tuple:
@@ -80,8 +100,9 @@ def _varlen_lengths(seed: int, nseq: int, lo: int, hi: int) -> tuple:
 
 
 def _mk(name, dtype, B, H, N, D, causal, seed, qk_std=1.0, generator="default_rng", varlen=None,
-        len_draw=None):
-    return Workload(name, dtype, B, H, N, D, causal, seed, qk_std, generator, varlen, len_draw)
+        len_draw=None, Nk=None, varlen_k=None):
+    return Workload(name, dtype, B, H, N, D, causal, seed, qk_std, generator, varlen, len_draw,
+                    Nk, varlen_k)
 
 
 def _varlen_workload() -> Workload:
@@ -104,14 +125,37 @@ WORKLOADS = {
 # The workload the throughput line is quoted on (bf16, causal, D=128, N=8192).
 HEADLINE = "bf16_causal_b2_h32_n8192_d128"
 
+# Cross-attention cases: a 2048-token chunk of queries against 8192 keys
+# (the chunk's own keys are the last 2048, so causal alignment is bottom-right),
+# and 8192 queries against a 1024-key memory without a mask.
+CROSS_WORKLOADS = {
+    "bf16_cross_causal_b2_h32_nq2048_nk8192_d128": _mk(
+        "bf16_cross_causal_b2_h32_nq2048_nk8192_d128", "bf16", 2, 32, 2048, 128, True, 0,
+        Nk=8192),
+    "bf16_cross_b2_h32_nq8192_nk1024_d128": _mk(
+        "bf16_cross_b2_h32_nq8192_nk1024_d128", "bf16", 2, 32, 8192, 128, False, 0, Nk=1024),
+}
+
 
 def custom(dtype="bf16", B=1, H=1, N=128, D=128, causal=True, seed=0, qk_std=1.0,
-           varlen=None, name="custom") -> Workload:
-    """A workload of arbitrary shape drawn with the default_rng recipe."""
+           varlen=None, name="custom", Nk=None, varlen_k=None) -> Workload:
+    """A workload of arbitrary shape drawn with the default_rng recipe.
+
+    ``Nk`` (dense) or ``varlen_k`` (packed, one key length per sequence) gives
+    the keys another length than the queries.
+    """
     if varlen is not None:
         varlen = tuple(int(x) for x in varlen)
         B, N = len(varlen), int(sum(varlen))
-    return _mk(name, dtype, B, H, N, D, causal, seed, qk_std, "default_rng", varlen)
+        if varlen_k is not None:
+            varlen_k = tuple(int(x) for x in varlen_k)
+            if len(varlen_k) != len(varlen):
+                raise ValueError("varlen_k needs one length per sequence")
+            Nk = int(sum(varlen_k))
+    elif varlen_k is not None:
+        raise ValueError("varlen_k needs varlen")
+    return _mk(name, dtype, B, H, N, D, causal, seed, qk_std, "default_rng", varlen, Nk=Nk,
+               varlen_k=varlen_k)
 
 
 def cu_seqlens_of(lengths) -> np.ndarray:
@@ -143,11 +187,12 @@ def generate(w: Workload, as_torch=True):
     """
     import torch
     shape = (w.H, w.N, w.D) if w.varlen is not None else (w.B, w.H, w.N, w.D)
+    kshape = shape[:-2] + (w.n_keys, w.D)
     if w.generator == "legacy":
         np.random.seed(w.seed)
         q = np.random.randn(*shape).astype(np.float32)
-        k = np.random.randn(*shape).astype(np.float32)
-        v = np.random.randn(*shape).astype(np.float32)
+        k = np.random.randn(*kshape).astype(np.float32)
+        v = np.random.randn(*kshape).astype(np.float32)
     else:
         rng = np.random.default_rng(w.seed)
         if w.len_draw is not None:
@@ -155,8 +200,8 @@ def generate(w: Workload, as_torch=True):
             nseq, lo, hi = w.len_draw
             rng.integers(lo, hi + 1, size=nseq)
         q = rng.standard_normal(shape, dtype=np.float32)
-        k = rng.standard_normal(shape, dtype=np.float32)
-        v = rng.standard_normal(shape, dtype=np.float32)
+        k = rng.standard_normal(kshape, dtype=np.float32)
+        v = rng.standard_normal(kshape, dtype=np.float32)
     if w.qk_std != 1.0:
         q *= np.float32(w.qk_std)
         k *= np.float32(w.qk_std)
@@ -167,7 +212,8 @@ def generate(w: Workload, as_torch=True):
     else:
         tq, tk, tv = (torch.from_numpy(np.ascontiguousarray(a)) for a in (q, k, v))
     cu = cu_seqlens_of(w.varlen) if w.varlen is not None else None
-    return {"q": tq, "k": tk, "v": tv, "cu_seqlens": cu, "shape": shape}
+    cuk = cu_seqlens_of(w.varlen_k) if w.varlen_k is not None else None
+    return {"q": tq, "k": tk, "v": tv, "cu_seqlens": cu, "cu_seqlens_k": cuk, "shape": shape}
 
 
 def as_f64(t) -> np.ndarray:

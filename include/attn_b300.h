@@ -53,7 +53,7 @@ extern "C" {
 
 typedef enum {
   ATTN_OK = 0,
-  ATTN_ERR_NULL = -1,     /* a required pointer is NULL                                */
+  ATTN_ERR_NULL = -1,     /* a required pointer is NULL (or only one of cu_seqlens_q/_k) */
   ATTN_ERR_SHAPE = -2,    /* B < 1, H < 1, N < 0, or sizes overflow the index types    */
   ATTN_ERR_HEADDIM = -3,  /* D not supported by this entry point                       */
   ATTN_ERR_ALIGN = -4,    /* q/k/v/o not 16-byte aligned, lse/cu_seqlens not 4-byte     */
@@ -62,9 +62,13 @@ typedef enum {
   ATTN_ERR_TIMEOUT = -7,  /* (device) a bounded wait inside a kernel ran out of time    */
   ATTN_ERR_BOUNDS = -8,   /* (device) cu_seqlens entries outside [0, N] or decreasing   */
   ATTN_ERR_SCALE = -9,    /* scale is not a finite number > 0                           */
-  ATTN_ERR_SCRATCH = -10  /* attn_decode_noalloc: the problem needs more than the built-in
+  ATTN_ERR_SCRATCH = -10, /* attn_decode_noalloc: the problem needs more than the built-in
                              scratch (ATTN_NOALLOC_SCRATCH_BYTES)                        */
+  ATTN_ERR_DTYPE = -11    /* attn_fwd_cross: element type not one of attn_dtype          */
 } attn_status;
+
+/* Element type of q, k, v and o for attn_fwd_cross. */
+typedef enum { ATTN_BF16 = 0, ATTN_F16 = 1, ATTN_F32 = 2 } attn_dtype;
 
 /*
  * bf16 forward on tcgen05 tensor cores.
@@ -100,6 +104,36 @@ int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* ls
 int attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
                  int H, int N, int D, const int* cu_seqlens, int causal, float scale,
                  void* stream);
+
+/*
+ * Forward with queries and keys of different lengths (cross-attention, which
+ * "Python Attention Mechanisms Explained: From Self-Attention to Flash
+ * Attention" names in section "The Core Idea").  The pages fix no mask for
+ * this case; the causal mask here aligns the LAST query with the LAST key:
+ * key j is allowed for query i when j <= i + (Nk - Nq).  With Nq < Nk the
+ * queries are thus the last Nq positions of an Nk-long sequence and the
+ * result equals the last Nq rows of causal self-attention over all Nk
+ * positions; with Nq > Nk the first Nq - Nk queries see no key and get
+ * O = 0, LSE = -inf.  Without the mask every query sees every key.
+ *   dense  (cu_seqlens_q == cu_seqlens_k == NULL): q, o are (B, H, Nq, D),
+ *          lse is (B, H, Nq); k, v are (B, H, Nk, D).
+ *   packed (both non-NULL, DEVICE int32, B+1 entries each): q, o are
+ *          (H, Nq, D) and lse (H, Nq) with Nq the total query tokens; k, v
+ *          are (H, Nk, D) with Nk the total key tokens.  Sequence s has
+ *          queries [cu_seqlens_q[s], cu_seqlens_q[s+1]) and keys
+ *          [cu_seqlens_k[s], cu_seqlens_k[s+1]); the causal alignment is per
+ *          sequence.  Passing only one of the two arrays is ATTN_ERR_NULL.
+ *   dtype : ATTN_BF16 or ATTN_F16 (D in {64, 128}, tensor cores, the
+ *          arithmetic of attn_fwd / attn_fwd_f16) or ATTN_F32 (1 <= D <= 128,
+ *          the arithmetic of attn_fwd_f32).
+ * Nk == 0 (or a sequence without keys) is allowed: those queries see no key,
+ * and k, v may be NULL when Nk == 0.  attn_fwd, attn_fwd_f16 and attn_fwd_f32
+ * are this call with Nk == Nq and cu_seqlens_k == cu_seqlens_q.  Device-side
+ * checks, ownership and errors are as for attn_fwd.
+ */
+int attn_fwd_cross(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int H, int Nq, int Nk, int D, const int* cu_seqlens_q,
+                   const int* cu_seqlens_k, int causal, float scale, int dtype, void* stream);
 
 /*
  * KV-cache decode (bf16): Nq new query rows per (batch, head) attend to all Nk

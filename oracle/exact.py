@@ -114,7 +114,7 @@ def attention_plane(qp, kp, vp, scale, causal, offset=None):
     return o, lse
 
 
-def _planes(q, k, v, cu_seqlens):
+def _planes(q, k, v, cu_seqlens, cu_seqlens_k):
     """Yield (index, q-plane, k-plane, v-plane) views for dense or packed layouts."""
     if cu_seqlens is None:
         B, H = q.shape[0], q.shape[1]
@@ -123,23 +123,27 @@ def _planes(q, k, v, cu_seqlens):
                 yield (b, h, slice(None)), q[b, h], k[b, h], v[b, h]
     else:
         cu = np.asarray(cu_seqlens, dtype=np.int64)
+        cuk = cu if cu_seqlens_k is None else np.asarray(cu_seqlens_k, dtype=np.int64)
         H = q.shape[0]
         for s in range(len(cu) - 1):
             a, e = int(cu[s]), int(cu[s + 1])
+            ak, ek = int(cuk[s]), int(cuk[s + 1])
             for h in range(H):
-                yield (None, h, slice(a, e)), q[h, a:e], k[h, a:e], v[h, a:e]
+                yield (None, h, slice(a, e)), q[h, a:e], k[h, ak:ek], v[h, ak:ek]
 
 
-def attention(q, k, v, scale, causal, cu_seqlens=None):
+def attention(q, k, v, scale, causal, cu_seqlens=None, cu_seqlens_k=None):
     """Exact attention forward in fp64.
 
-    q, k, v: float arrays, (B, H, N, D) dense or (H, N_total, D) packed.
+    q, k, v: float arrays, (B, H, N, D) dense or (H, N_total, D) packed; k and
+    v may hold a different number of rows (Nk) than q, and in the packed form
+    their own offsets ``cu_seqlens_k`` (default: ``cu_seqlens``).
     Returns (O, LSE): O with q's shape, LSE with q's shape minus the last axis.
     """
     q, k, v = (np.asarray(a, dtype=np.float64) for a in (q, k, v))
     o = np.empty(q.shape[:-1] + (v.shape[-1],), dtype=np.float64)
     lse = np.empty(q.shape[:-1], dtype=np.float64)
-    for (b, h, sl), qp, kp, vp in _planes(q, k, v, cu_seqlens):
+    for (b, h, sl), qp, kp, vp in _planes(q, k, v, cu_seqlens, cu_seqlens_k):
         po, pl = attention_plane(qp, kp, vp, scale, causal)
         if b is None:
             o[h, sl], lse[h, sl] = po, pl

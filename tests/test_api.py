@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_version_and_strerror(lib):
     assert B.attn_version() >= 100
-    for code in range(-9, 1):
+    for code in range(-11, 1):
         s = B.strerror(code)
         assert s and s != "unknown status"
     assert B.strerror(-1234) == "unknown status"
@@ -73,6 +73,33 @@ def test_argument_errors_return_before_launch(lib, fn):
     assert call(N=0, q=None, k=None, v=None, o=None, lse=None) == B.ATTN_OK
 
 
+@pytest.mark.parametrize("dtype", [B.ATTN_BF16, B.ATTN_F16, B.ATTN_F32])
+def test_cross_argument_errors(lib, dtype):
+    def call(**kw):
+        a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, H=2, Nq=16, Nk=40, D=64, cq=None, ck=None,
+                 causal=1, scale=0.125, dtype=dtype)
+        a.update(kw)
+        return B.attn_fwd_cross(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"],
+                                a["Nq"], a["Nk"], a["D"], a["cq"], a["ck"], a["causal"],
+                                a["scale"], a["dtype"], None)
+    assert call(Nq=-1) == B.ATTN_ERR_SHAPE
+    assert call(Nk=-1) == B.ATTN_ERR_SHAPE
+    assert call(B=0) == B.ATTN_ERR_SHAPE
+    assert call(cq=P) == B.ATTN_ERR_NULL          # only one of the two offset arrays
+    assert call(ck=P) == B.ATTN_ERR_NULL
+    assert call(k=None) == B.ATTN_ERR_NULL
+    assert call(v=None) == B.ATTN_ERR_NULL
+    assert call(cq=P, ck=P + 2) == B.ATTN_ERR_ALIGN
+    assert call(k=P + 8) == B.ATTN_ERR_ALIGN
+    assert call(scale=0.0) == B.ATTN_ERR_SCALE
+    assert call(D=129) == B.ATTN_ERR_HEADDIM
+    assert call(dtype=3) == B.ATTN_ERR_DTYPE
+    assert call(dtype=-1) == B.ATTN_ERR_DTYPE
+    # Nq == 0 is a no-op; Nk == 0 accepts NULL k and v (then fails only for want of a GPU)
+    assert call(Nq=0, q=None, k=None, v=None, o=None, lse=None) == B.ATTN_OK
+    assert call(Nk=0, k=None, v=None) in (B.ATTN_OK, B.ATTN_ERR_LAUNCH)
+
+
 def test_16bit_head_dims(lib):
     for fn in (B.attn_fwd, B.attn_fwd_f16):
         for d in (32, 96, 256):
@@ -93,6 +120,9 @@ def test_no_device_means_loud_failure(lib):
     assert B.attn_fwd(P, P, P, P, P, 1, 1, 16, 64, None, 1, 0.125, None) == B.ATTN_ERR_LAUNCH
     assert B.attn_fwd_f16(P, P, P, P, P, 1, 1, 16, 64, None, 1, 0.125, None) == B.ATTN_ERR_LAUNCH
     assert B.attn_fwd_f32(P, P, P, P, P, 1, 1, 16, 64, None, 1, 0.125, None) == B.ATTN_ERR_LAUNCH
+    for dt in (B.ATTN_BF16, B.ATTN_F16, B.ATTN_F32):
+        assert B.attn_fwd_cross(P, P, P, P, P, 1, 1, 16, 48, 64, None, None, 1, 0.125, dt,
+                                None) == B.ATTN_ERR_LAUNCH
 
 
 def test_decode_argument_errors(lib):

@@ -125,3 +125,37 @@ def test_varlen_lengths_from_seed_7():
 def test_workload_config_keys(name):
     cfg = bench.workload_config(W.WORKLOADS[name])
     assert cfg["workload"] == name and cfg["flops_per_step"] > 0
+
+
+def test_cross_flop_counts_follow_the_pair_count():
+    # 4*D flops per allowed (query, key) pair; the causal count drops the
+    # diagonal's half pair per row, as the self-attention N^2/2 convention does
+    for nq, nk, causal in ((2048, 8192, True), (8192, 1024, False), (300, 77, True),
+                           (77, 300, True)):
+        w = W.custom("bf16", B=2, H=3, N=nq, D=64, causal=causal, Nk=nk)
+        i = np.arange(nq)
+        exact = np.clip(i + 1 + nk - nq, 0, nk).sum() if causal else nq * nk
+        assert abs(w.flops() - 4 * 64 * 6 * exact) <= 4 * 64 * 6 * (nq / 2 + 1e-9)
+    w = W.CROSS_WORKLOADS["bf16_cross_causal_b2_h32_nq2048_nk8192_d128"]
+    assert w.flops() == 4 * 128 * 64 * (2048 * 8192 - 2048 ** 2 / 2)
+
+
+def test_cross_generator_shapes():
+    w = W.custom("bf16", B=2, H=3, N=40, D=64, Nk=70, seed=1)
+    x = W.generate(w)
+    assert tuple(x["q"].shape) == (2, 3, 40, 64) and tuple(x["k"].shape) == (2, 3, 70, 64)
+    assert tuple(x["v"].shape) == (2, 3, 70, 64)
+    p = W.generate(W.custom("f32", H=2, D=16, varlen=[3, 0, 5], varlen_k=[4, 2, 0]))
+    assert tuple(p["q"].shape) == (2, 8, 16) and tuple(p["k"].shape) == (2, 6, 16)
+    assert list(p["cu_seqlens"]) == [0, 3, 3, 8] and list(p["cu_seqlens_k"]) == [0, 4, 6, 6]
+    # with Nk == N the draw is the self-attention draw
+    a = W.generate(W.custom("bf16", B=1, H=2, N=33, D=64, seed=5))
+    b = W.generate(W.custom("bf16", B=1, H=2, N=33, D=64, seed=5, Nk=33))
+    for key in ("q", "k", "v"):
+        assert (a[key].float() == b[key].float()).all()
+
+
+@pytest.mark.parametrize("name", sorted(W.CROSS_WORKLOADS))
+def test_cross_workload_config_keys(name):
+    cfg = bench.workload_config(W.CROSS_WORKLOADS[name])
+    assert cfg["workload"] == name and cfg["Nk"] == W.CROSS_WORKLOADS[name].n_keys

@@ -433,3 +433,22 @@ def test_cross_rows_equal_plane():
     ro, rl = A.attention_rows(q, k, v, 0.3, True, rows)
     np.testing.assert_allclose(ro, o[rows], rtol=0, atol=1e-13)
     np.testing.assert_allclose(rl, lse[rows], rtol=0, atol=1e-13)
+
+
+def test_packed_cross_equals_per_sequence_dense():
+    rng = np.random.default_rng(44)
+    lq, lk = [3, 0, 130, 5, 1], [7, 4, 100, 0, 1]
+    cq, ck = np.cumsum([0] + lq), np.cumsum([0] + lk)
+    H, d = 2, 8
+    q, k, v = _rand(rng, H, cq[-1], d), _rand(rng, H, ck[-1], d), _rand(rng, H, ck[-1], d)
+    for causal in (False, True):
+        o, lse = A.attention(q, k, v, 0.3, causal, cu_seqlens=cq, cu_seqlens_k=ck)
+        for s in range(len(lq)):
+            for h in range(H):
+                qa, qe, ka, ke = cq[s], cq[s + 1], ck[s], ck[s + 1]
+                ro, rl = _brute_causal_cross(q[h, qa:qe], k[h, ka:ke], v[h, ka:ke], 0.3) if causal \
+                    else A.attention_plane(q[h, qa:qe], k[h, ka:ke], v[h, ka:ke], 0.3, False)
+                np.testing.assert_allclose(o[h, qa:qe], ro, rtol=0, atol=1e-12)
+                assert np.array_equal(np.isneginf(lse[h, qa:qe]), np.isneginf(rl))
+        # a sequence with no keys: its queries get O = 0, LSE = -inf
+        assert (o[:, cq[3]:cq[4]] == 0).all() and np.isneginf(lse[:, cq[3]:cq[4]]).all()
