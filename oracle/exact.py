@@ -52,6 +52,9 @@ Mechanisms Explained", "The Core Idea"); this bottom-right alignment makes a
 cross call on the last Nq queries equal the last Nq rows of self-attention.
 A row with no allowed key has O = 0 and LSE = -inf.
 
+The backward pass (dQ, dK, dV for an upstream gradient dO) is the plain
+gradient of the same definition; see the section "Backward pass" below.
+
 Layouts match the CUDA boundary: dense tensors are (B, H, N, D); packed
 variable-length tensors are (H, N_total, D) with ``cu_seqlens`` of length
 nseq+1, each sequence attending only to itself with positions relative to its
@@ -221,3 +224,94 @@ def online_tiled(qp, kp, vp, scale, causal, br=128, bc=128):
         o[i0:i1] = np.where(live[:, None], acc / np.where(live, l, 1.0)[:, None], 0.0)
         lse[i0:i1] = np.where(live, m + np.log(np.where(live, l, 1.0)), -np.inf)
     return o, lse
+
+
+# ---------------------------------------------------------------------------
+# Backward pass
+# ---------------------------------------------------------------------------
+#
+# The pages name the backward pass as the next extension of the forward
+# kernel: keep the forward's softmax statistics and output, and rebuild the
+# probabilities tile by tile while the gradients stream back ("Building a
+# FlashAttention-2 forward kernel in pure NumPy", section "Extending It: Your
+# Roadmap to Senior-Level").  What it computes is the plain gradient of the forward
+# above for a scalar loss whose gradient with respect to O is dO:
+#
+#     dV   = P^T dO
+#     dP   = dO V^T
+#     dS   = P * (dP - Delta),   Delta_i = sum_j P_ij dP_ij = dO_i . O_i
+#     dQ   = scale * dS K
+#     dK   = scale * dS^T Q
+#
+# (the softmax Jacobian applied row by row; masked entries have P = 0 and so
+# dS = 0; a query with no allowed key has a constant O = 0 and contributes
+# nothing).  The oracle materialises P from the definition, as the forward
+# does; it is pinned by central finite differences of the forward and by
+# the identities sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i.
+
+
+def _probs_rows(qp, kp, scale, causal, offset, r0, r1):
+    """Rows [r0, r1) of the probability matrix P of one plane (zeros for rows with no key)."""
+    n_keys = kp.shape[0]
+    s = scale * (qp[r0:r1] @ kp.T)
+    if causal:
+        i = np.arange(r0, r1)[:, None]
+        j = np.arange(n_keys)[None, :]
+        s = np.where(j <= i + offset, s, -np.inf)
+    p = np.zeros_like(s)
+    live = np.isfinite(s).any(axis=1) if n_keys else np.zeros(r1 - r0, dtype=bool)
+    if live.any():
+        sl = s[live]
+        e = np.exp(sl - sl.max(axis=1, keepdims=True))
+        p[live] = e / e.sum(axis=1, keepdims=True)
+    return p
+
+
+def attention_backward_plane(qp, kp, vp, dop, scale, causal, offset=None):
+    """dQ, dK, dV of one plane in fp64 (qp, dop: (Nq, D); kp, vp: (Nk, D)).
+
+    Long planes are processed in query-row slabs; every slab's contribution
+    to dK and dV is summed, which is the same matrix product split by rows.
+    """
+    qp, kp, vp, dop = (np.asarray(a, dtype=np.float64) for a in (qp, kp, vp, dop))
+    n = qp.shape[0]
+    if offset is None:
+        offset = kp.shape[0] - n
+    dq = np.zeros_like(qp)
+    dk = np.zeros_like(kp)
+    dv = np.zeros_like(vp)
+    step = max(1, n if n <= FULL_MATRIX_MAX_N else SLAB_ROWS)
+    for r0 in range(0, n, step):
+        r1 = min(n, r0 + step)
+        p = _probs_rows(qp, kp, scale, causal, offset, r0, r1)     # (rows, Nk)
+        o = p @ vp
+        dv += p.T @ dop[r0:r1]
+        dp = dop[r0:r1] @ vp.T
+        delta = (dop[r0:r1] * o).sum(axis=1, keepdims=True)
+        ds = p * (dp - delta)
+        dq[r0:r1] = scale * (ds @ kp)
+        dk += scale * (ds.T @ qp[r0:r1])
+    return dq, dk, dv
+
+
+def attention_backward(q, k, v, do, scale, causal, cu_seqlens=None, cu_seqlens_k=None):
+    """dQ, dK, dV in fp64 for dense (B, H, N, D) or packed (H, N_total, D) tensors
+    (the layouts of :func:`attention`)."""
+    q, k, v, do = (np.asarray(a, dtype=np.float64) for a in (q, k, v, do))
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    if cu_seqlens is None:
+        for b in range(q.shape[0]):
+            for h in range(q.shape[1]):
+                dq[b, h], dk[b, h], dv[b, h] = attention_backward_plane(
+                    q[b, h], k[b, h], v[b, h], do[b, h], scale, causal)
+    else:
+        cu = np.asarray(cu_seqlens, dtype=np.int64)
+        cuk = cu if cu_seqlens_k is None else np.asarray(cu_seqlens_k, dtype=np.int64)
+        for s in range(len(cu) - 1):
+            a, e, ak, ek = int(cu[s]), int(cu[s + 1]), int(cuk[s]), int(cuk[s + 1])
+            for h in range(q.shape[0]):
+                dq[h, a:e], dk[h, ak:ek], dv[h, ak:ek] = attention_backward_plane(
+                    q[h, a:e], k[h, ak:ek], v[h, ak:ek], do[h, a:e], scale, causal)
+    return dq, dk, dv
