@@ -416,6 +416,71 @@ def run_ours(args, w):
     return 0
 
 
+def run_backward(args, w):
+    """Backward pass (a NEXT row): device-timed TFLOP/s, 2.5x the forward's FLOPs
+    (five matrix products per tile pair instead of two)."""
+    import torch
+    from exact_io_aware_107_b300 import (_binding, attention_backward, attention_forward,
+                                         device_error)
+
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _binding.load()
+    x = W.generate(w)
+    q, k, v = (t.to(dev) for t in (x["q"], x["k"], x["v"]))
+    rng = np.random.default_rng(1)
+    do = torch.from_numpy(rng.standard_normal(tuple(q.shape), dtype=np.float32)).to(q.dtype).to(dev)
+    cu = None if x["cu_seqlens"] is None else torch.as_tensor(x["cu_seqlens"]).to(dev)
+    cuk = None if x["cu_seqlens_k"] is None else torch.as_tensor(x["cu_seqlens_k"]).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    o, lse = attention_forward(q, k, v, causal=w.causal, scale=w.scale, cu_seqlens=cu,
+                               cu_seqlens_k=cuk, stream=stream)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    rc, nbytes = _binding.attn_bwd_workspace_bytes(w.B, w.H, w.N, w.D, cu is not None)
+    assert rc == 0
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+
+    def step():
+        attention_backward(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, cu_seqlens=cu,
+                           cu_seqlens_k=cuk, dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    if device_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    ms = sum(s_.elapsed_time(e) for s_, e in zip(starts, ends)) / args.steps
+    flops = 2.5 * w.flops()
+    peak_tf, _, peak_kind = load_peaks()
+    tf = flops / (ms * 1e-3) / 1e12
+    print(f"[bench] backward {w.name}: {ms:.3f} ms/step, {tf:.1f} TFLOP/s", file=sys.stderr)
+    line = {
+        "metric": "attention bwd TFLOPS (bf16, 2.5x forward FLOPs)", "value": tf,
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic", "config": workload_config(w),
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": tf / peak_tf, "peak_source": f"{peak_kind} cuBLAS bf16 burst",
+                     "kernel": f"attn_bwd_bf16_kernel<{w.D}> (+ prep and dQ kernels)",
+                     "traffic": None},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def run_decode(args):
     """KV-cache decode (a NEXT row): device-timed GB/s against the HBM roofline."""
     import torch
@@ -482,8 +547,9 @@ def main(argv=None):
     ap.add_argument("--workload", default=W.HEADLINE,
                     choices=sorted(W.WORKLOADS) + sorted(W.CROSS_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["forward", "decode"], default="forward",
-                    help="decode: the KV-cache decode path (GB/s against HBM)")
+    ap.add_argument("--op", choices=["forward", "backward", "decode"], default="forward",
+                    help="backward: dQ, dK, dV (TFLOP/s); decode: the KV-cache decode path "
+                         "(GB/s against HBM)")
     ap.add_argument("--decode-shape", default="8,32,1,32768,128", help="B,H,Nq,Nk,D for --op decode")
     ap.add_argument("--shape", default=None,
                     help="B,H,N,D (or B,H,Nq,Nk,D for cross-attention): same dtype and mask "
@@ -507,6 +573,8 @@ def main(argv=None):
                                  f"{'causal_' if w.causal else ''}b{b}_h{h}_{tag}_d{d}")
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.op == "backward":
+        return run_backward(args, w)
     return run_ours(args, w)
 
 

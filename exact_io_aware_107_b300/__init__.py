@@ -18,7 +18,8 @@ import math
 from . import _binding
 from ._binding import AttnError
 
-__all__ = ["attention_forward", "attention_decode", "AttnError", "device_error", "load_library"]
+__all__ = ["attention_forward", "attention_backward", "attention_decode", "AttnError",
+           "device_error", "load_library"]
 
 
 def load_library():
@@ -106,6 +107,66 @@ def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens=None, out=No
     if rc != _binding.ATTN_OK:
         raise AttnError(rc, where)
     return out, lse
+
+
+def attention_backward(q, k, v, o, lse, dout, causal=False, scale=None, cu_seqlens=None,
+                       cu_seqlens_k=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV of the forward for the upstream gradient ``dout``.
+
+    q, k, v, causal, scale, cu_seqlens, cu_seqlens_k: as passed to
+    :func:`attention_forward`; o, lse: its outputs.  bf16 or fp16, D in {64, 128}.
+    ``workspace``: a CUDA tensor of at least ``attn_bwd_workspace_bytes``
+    bytes, or None to let torch allocate one here (the library itself never
+    allocates).  Returns (dQ, dK, dV).
+    """
+    import torch
+
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("the backward takes bfloat16 or float16 tensors")
+    for t in (q, k, v, o, dout):
+        if t.dtype != q.dtype or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v, o, dout must be contiguous CUDA tensors of one dtype")
+    if o.shape != q.shape or dout.shape != q.shape or k.shape != v.shape:
+        raise ValueError("o and dout must be shaped like q, v like k")
+    if lse.dtype != torch.float32 or lse.shape != q.shape[:-1] or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 shaped like q without its last axis")
+    cu_q = None if cu_seqlens is None else cu_seqlens.contiguous()
+    cu_k = None if cu_seqlens_k is None else cu_seqlens_k.contiguous()
+    if cu_q is None:
+        if cu_k is not None:
+            raise ValueError("cu_seqlens_k needs cu_seqlens")
+        B, H, N, D = q.shape
+        Nk = k.shape[2]
+        if k.shape != (B, H, Nk, D):
+            raise ValueError("k, v must be (B, H, Nk, D) with q's B, H, D")
+    else:
+        H, N, D = q.shape
+        B = cu_q.numel() - 1
+        Nk = k.shape[1]
+        if k.shape != (H, Nk, D):
+            raise ValueError("k, v must be (H, Nk_total, D) with q's H, D")
+        if cu_k is None:
+            cu_k = cu_q
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        rc, nbytes = _binding.attn_bwd_workspace_bytes(B, H, N, D, cu_q is not None)
+        if rc != _binding.ATTN_OK:
+            raise AttnError(rc, "attention_backward")
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    dtype = _binding.ATTN_BF16 if q.dtype == torch.bfloat16 else _binding.ATTN_F16
+    rc = _binding.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                           _ptr(dk), _ptr(dv), B, H, N, Nk, D, _ptr(cu_q), _ptr(cu_k), causal,
+                           scale, dtype, _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), stream.cuda_stream)
+    if rc != _binding.ATTN_OK:
+        raise AttnError(rc, "attention_backward")
+    return dq, dk, dv
 
 
 def attention_decode(q, k, v, scale=None, workspace=None, out=None, lse=None, stream=None):

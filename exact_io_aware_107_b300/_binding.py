@@ -45,6 +45,11 @@ _SIGNATURES = {
     "attn_fwd_cross": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
                        + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
                           ctypes.c_int, ctypes.c_void_p]),
+    "attn_bwd": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 5
+                 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                    ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_void_p]),
+    "attn_bwd_workspace_bytes": (ctypes.c_int, [ctypes.c_int] * 5
+                                 + [ctypes.POINTER(ctypes.c_ulonglong)]),
     "attn_decode": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
                     + [ctypes.c_float, ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_void_p]),
     "attn_decode_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
@@ -114,6 +119,22 @@ def attn_fwd_cross(q, k, v, o, lse, B, H, Nq, Nk, D, cu_seqlens_q, cu_seqlens_k,
     return load().attn_fwd_cross(q, k, v, o, lse, int(B), int(H), int(Nq), int(Nk), int(D),
                                  cu_seqlens_q, cu_seqlens_k, int(causal), float(scale),
                                  int(dtype), stream)
+
+
+def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, D, cu_seqlens_q, cu_seqlens_k,
+             causal, scale, dtype, workspace, workspace_bytes, stream) -> int:
+    """Backward pass (dQ, dK, dV); pointers are ints (device addresses) or None."""
+    return load().attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, int(B), int(H), int(Nq), int(Nk),
+                           int(D), cu_seqlens_q, cu_seqlens_k, int(causal), float(scale),
+                           int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def attn_bwd_workspace_bytes(B, H, Nq, D, packed):
+    """(status, bytes) for the backward workspace."""
+    n = ctypes.c_ulonglong(0)
+    rc = load().attn_bwd_workspace_bytes(int(B), int(H), int(Nq), int(D), int(bool(packed)),
+                                         ctypes.byref(n))
+    return rc, n.value
 
 
 def attn_decode(q, k, v, o, lse, B, H, Nq, Nk, D, scale, workspace, workspace_bytes,

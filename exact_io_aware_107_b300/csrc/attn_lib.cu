@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "../../include/attn_b300.h"
+#include "bwd_bf16_sm103.cuh"
 #include "decode_bf16.cuh"
 #include "fwd_bf16_sm103.cuh"
 #include "fwd_f32.cuh"
@@ -133,6 +134,21 @@ int prepare_device(DeviceState** out) {
     if (set_decode_smem<64, 1>() || set_decode_smem<64, 2>() || set_decode_smem<64, 4>() ||
         set_decode_smem<64, 8>() || set_decode_smem<128, 1>() || set_decode_smem<128, 2>() ||
         set_decode_smem<128, 4>() || set_decode_smem<128, 8>()) {
+      cudaGetLastError();
+      return ATTN_ERR_LAUNCH;
+    }
+    if (cudaFuncSetAttribute(attn_bwd_bf16_kernel<64, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             BwdCfg<64>::SMEM_ALLOC) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_bwd_bf16_kernel<128, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             BwdCfg<128>::SMEM_ALLOC) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_bwd_bf16_kernel<64, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             BwdCfg<64>::SMEM_ALLOC) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_bwd_bf16_kernel<128, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             BwdCfg<128>::SMEM_ALLOC) != cudaSuccess) {
       cudaGetLastError();
       return ATTN_ERR_LAUNCH;
     }
@@ -314,6 +330,121 @@ int fwd_any(const void* q, const void* k, const void* v, void* o, float* lse, in
     default:
       return ATTN_ERR_DTYPE;
   }
+}
+
+// Workspace of the backward: Delta (fp32 per query row, padded to 256 bytes)
+// followed by the fp32 dQ accumulator.
+size_t bwd_delta_bytes(long long qrows) {
+  return ((static_cast<size_t>(qrows) * 4 + 255) / 256) * 256;
+}
+size_t bwd_workspace_bytes(long long planes, long long nq, int D) {
+  return bwd_delta_bytes(planes * nq) + static_cast<size_t>(planes * nq) * D * 4;
+}
+
+template <int D, bool F16>
+void launch_bwd_kernels(unsigned grid, cudaStream_t s, const CUtensorMap& mq,
+                        const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
+                        const BwdParams& p, long long qrows) {
+  if (qrows > 0) {
+    const long long threads = qrows * 16;
+    attn_bwd_prep_kernel<D, F16><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(
+        p, qrows);
+  }
+  if (grid > 0)
+    attn_bwd_bf16_kernel<D, F16><<<grid, BwdCfg<D>::THREADS, BwdCfg<D>::SMEM_ALLOC, s>>>(
+        mq, mk, mv, mdo, p);
+  if (qrows > 0) {
+    const long long n8 = qrows * D / 8;
+    attn_bwd_dq_kernel<F16><<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(p, n8);
+  }
+}
+
+int bwd_16bit(const void* q, const void* k, const void* v, const void* o, const float* lse,
+              const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int D,
+              const int* cu_q, const int* cu_k, int causal, float scale, bool f16,
+              void* workspace, unsigned long long workspace_bytes, cudaStream_t s) {
+  if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+  const int planes = cu_q ? H : B * H;
+  const long long qrows = 1LL * planes * Nq;
+  if (qrows > 0) {
+    if (!q || !dout || !dq || !o || !lse || !workspace) return ATTN_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(dout, 16) || !aligned(dq, 16) || !aligned(o, 16) ||
+        !aligned(lse, 4) || !aligned(workspace, 16))
+      return ATTN_ERR_ALIGN;
+    if (workspace_bytes < bwd_workspace_bytes(planes, Nq, D)) return ATTN_ERR_SCRATCH;
+  }
+  if (Nk > 0) {
+    if (!k || !v || !dk || !dv) return ATTN_ERR_NULL;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(dk, 16) || !aligned(dv, 16))
+      return ATTN_ERR_ALIGN;
+  }
+  if ((cu_q && !aligned(cu_q, 4)) || (cu_k && !aligned(cu_k, 4))) return ATTN_ERR_ALIGN;
+  DeviceState* st = nullptr;
+  int rc = prepare_device(&st);
+  if (rc != ATTN_OK) return rc;
+
+  // With no key the main kernel has no tile: the prep and dQ kernels alone
+  // write dQ = 0.  With no query it writes dK = dV = 0 and reads no query.
+  CUtensorMap mq, mk, mv, mdo;
+  if (Nk > 0) {
+    if (encode_16bit_map(&mk, k, D, Nk, planes, f16) != ATTN_OK ||
+        encode_16bit_map(&mv, v, D, Nk, planes, f16) != ATTN_OK)
+      return ATTN_ERR_LAUNCH;
+  }
+  if (Nq > 0) {
+    if (encode_16bit_map(&mq, q, D, Nq, planes, f16) != ATTN_OK ||
+        encode_16bit_map(&mdo, dout, D, Nq, planes, f16) != ATTN_OK)
+      return ATTN_ERR_LAUNCH;
+  }
+  if (Nk == 0) {
+    mk = mq;
+    mv = mq;
+  }
+  if (Nq == 0) {
+    mq = mk;
+    mdo = mk;
+  }
+
+  BwdParams p;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.delta = static_cast<float*>(workspace);
+  p.dq_acc = workspace ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                  bwd_delta_bytes(qrows))
+                       : nullptr;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.cu_seqlens = cu_q;
+  p.cu_seqlens_k = cu_k;
+  p.nseq = cu_q ? B : 0;
+  p.planes = planes;
+  p.rows = Nq;
+  p.rows_k = Nk;
+  p.n_kblk = (Nk + 127) / 128;
+  const long long tiles = Nk == 0 ? 0 : (cu_q ? (1LL * (Nk / 128 + B)) : 1LL * p.n_kblk);
+  const long long grid = tiles * planes;
+  if (grid > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  p.n_tiles = static_cast<int>(tiles);
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = g_timeout_ns.load();
+  p.err = st->err;
+  const unsigned g = static_cast<unsigned>(grid);
+  if (D == 64) {
+    if (f16)
+      launch_bwd_kernels<64, true>(g, s, mq, mk, mv, mdo, p, qrows);
+    else
+      launch_bwd_kernels<64, false>(g, s, mq, mk, mv, mdo, p, qrows);
+  } else {
+    if (f16)
+      launch_bwd_kernels<128, true>(g, s, mq, mk, mv, mdo, p, qrows);
+    else
+      launch_bwd_kernels<128, false>(g, s, mq, mk, mv, mdo, p, qrows);
+  }
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 // Key slices per plane for the decode kernel: enough CTAs to cover every SM
@@ -504,6 +635,32 @@ extern "C" int attn_fwd_cross(const void* q, const void* k, const void* v, void*
                  dtype, stream);
 }
 
+extern "C" int attn_bwd_workspace_bytes(int B, int H, int Nq, int D, int packed,
+                                        unsigned long long* bytes) {
+  if (!bytes) return ATTN_ERR_NULL;
+  if (B < 1 || H < 1 || Nq < 0) return ATTN_ERR_SHAPE;
+  if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+  const long long planes = packed ? H : 1LL * B * H;
+  *bytes = Nq == 0 ? 0 : bwd_workspace_bytes(planes, Nq, D);
+  return ATTN_OK;
+}
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                        int H, int Nq, int Nk, int D, const int* cu_seqlens_q,
+                        const int* cu_seqlens_k, int causal, float scale, int dtype,
+                        void* workspace, unsigned long long workspace_bytes, void* stream) {
+  // the forward's checks cover q, k, v, the shapes, the offsets and the scale
+  // (o and lse stand in for the forward's outputs)
+  int rc = check_common(q, k, v, o, lse, B, H, Nq, Nk, cu_seqlens_q, cu_seqlens_k, scale);
+  if (rc != ATTN_OK) return rc;
+  if (dtype != ATTN_BF16 && dtype != ATTN_F16) return ATTN_ERR_DTYPE;
+  if (Nq == 0 && Nk == 0) return ATTN_OK;
+  return bwd_16bit(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, D, cu_seqlens_q,
+                   cu_seqlens_k, causal, scale, dtype == ATTN_F16, workspace, workspace_bytes,
+                   static_cast<cudaStream_t>(stream));
+}
+
 extern "C" const char* attn_strerror(int status) {
   switch (status) {
     case ATTN_OK: return "ok";
@@ -517,7 +674,7 @@ extern "C" const char* attn_strerror(int status) {
     case ATTN_ERR_BOUNDS: return "cu_seqlens entries outside [0, N] or decreasing";
     case ATTN_ERR_SCALE: return "scale must be finite and > 0";
     case ATTN_ERR_SCRATCH:
-      return "decode partials need more than the built-in scratch (ATTN_NOALLOC_SCRATCH_BYTES)";
+      return "the workspace (or the built-in decode scratch) is too small for this problem";
     case ATTN_ERR_DTYPE: return "element type not one of ATTN_BF16, ATTN_F16, ATTN_F32";
     default: return "unknown status";
   }

@@ -1,0 +1,629 @@
+// 16-bit (bf16 or fp16) attention backward for sm_103a: TMA + mbarrier
+// pipeline, tcgen05 MMAs with TMEM accumulators.
+//
+// What it computes is the gradient of the forward for an upstream gradient
+// dO, the backward pass that "Building a FlashAttention-2 forward kernel in
+// pure NumPy" names as the next extension ("Extending It: Your Roadmap to
+// Senior-Level"): the forward's log-sum-exp is kept, the probabilities are
+// rebuilt tile by tile from it (P_ij = exp(scale q_i.k_j - LSE_i)), and
+//
+//     dV = P^T dO,   dP = dO V^T,   dS = P * (dP - Delta),
+//     dQ = scale dS K,   dK = scale dS^T Q,   Delta_i = dO_i . O_i.
+//
+// Masked entries (the causal mask, aligned like the forward's: key j is
+// allowed for query i when j <= i + Nk - Nq) have P = 0 and so contribute
+// nothing.
+//
+// Three kernels run in order on the caller's stream:
+//   attn_bwd_prep_kernel   Delta_i = dO_i . O_i (fp32) and a zeroed fp32 dQ
+//                          accumulator, both in the caller's workspace;
+//   attn_bwd_bf16_kernel   one CTA per 128-key tile of one plane: it keeps
+//                          dK and dV for its keys in TMEM, streams the query
+//                          tiles that see those keys, and adds each tile's
+//                          dQ contribution to the fp32 accumulator;
+//   attn_bwd_dq_kernel     dQ = scale * accumulator, rounded once.
+//
+// CTA layout of the main kernel (320 threads):
+//   warps 0-3  "P/dS" warpgroup: thread t owns key row t (TMEM lane t).
+//              P^T = 2^(S^T * scale*log2e - LSE_q*log2e) goes back into TMEM
+//              as 16-bit pairs for the dV MMA; dS^T = P^T (dP^T - Delta_q) is
+//              written to shared memory for the dK and dQ MMAs.
+//   warps 4-7  "dQ" warpgroup: thread t owns query row t of the dQ tile;
+//              it reads the tile from TMEM and adds it to global memory with
+//              vector fp32 reductions.  At the end it writes dK.
+//   warp  8    tcgen05 MMA issuer and TMEM owner.
+//   warp  9    TMA producer (K, V once; Q and dO per query tile; the
+//              tile's LSE and Delta into shared memory).
+//
+// TMEM columns (fp32 cells, 128 lanes): dV [0, D), dK [D, 2D),
+// S^T [2D, 2D+128) (P^T overwrites its first 64 columns), dP^T
+// [2D+128, 2D+256); each tile's dQ (lanes = queries) reuses the dP^T columns
+// once the P/dS warpgroup has read dP^T.
+//
+// Shared memory: K, V (the CTA's keys), two Q stages, one dO stage, the dS
+// tile, and the per-stage LSE/Delta vectors.  Every 128 x D tile is stored as
+// TMA writes it: D/64 chunks of 128 rows x 128 bytes, 128-byte swizzled.  The
+// dS tile is written in the same format with keys as rows and queries along
+// the row, so the one buffer is both the K-major A operand of dK += dS^T Q
+// (M = keys) and the MN-major A operand of dQ = dS K (M = queries).
+//
+// MMA order per query tile i:  dP_i, [P_i ready] dV += P_i^T dO_i, S_{i+1},
+// [dS_i ready] dK += dS_i^T Q_i, dQ_i = dS_i K.  S_{i+1} overwrites the
+// columns P_i was read from, which the tensor pipe orders after the dV MMA.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace attn {
+
+struct BwdParams {
+  const void* o;            // forward output, layout of q (prep kernel)
+  const void* dout;         // upstream gradient, layout of q
+  const float* lse;         // forward log-sum-exp, natural log, layout (planes, rows)
+  float* delta;             // workspace: Delta, layout of lse
+  float* dq_acc;            // workspace: fp32 dQ accumulator, layout of q
+  void* dq;
+  void* dk;
+  void* dv;
+  const int* cu_seqlens;    // query offsets; nullptr for the dense layout
+  const int* cu_seqlens_k;  // key offsets (packed layout only)
+  int nseq;
+  int planes;               // dense: B*H; packed: H
+  int rows;                 // query rows per plane (dense Nq; packed total query tokens)
+  int rows_k;               // key rows per plane (dense Nk; packed total key tokens)
+  int n_kblk;               // dense: ceil(Nk/128)
+  int n_tiles;              // packed: an upper bound on the key tiles
+  int causal;
+  float scale;
+  float scale_log2;         // scale * log2(e)
+  unsigned long long timeout_ns;
+  unsigned int* err;
+};
+
+template <int D>
+struct BwdCfg {
+  static constexpr int BM = 128;                  // queries per tile
+  static constexpr int BN = 128;                  // keys per CTA
+  static constexpr int CHUNK_BYTES = 128 * 128;   // 128 rows x 128 bytes
+  static constexpr int NCHUNK = D / 64;
+  static constexpr int TILE_BYTES = 128 * D * 2;
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = TILE_BYTES;
+  static constexpr int Q_OFF = 2 * TILE_BYTES;    // two stages
+  static constexpr int DO_OFF = 4 * TILE_BYTES;   // one stage
+  static constexpr int DS_OFF = 5 * TILE_BYTES;
+  static constexpr int DS_BYTES = 2 * CHUNK_BYTES;  // 128 keys x 128 queries
+  static constexpr int STAT_OFF = DS_OFF + DS_BYTES;
+  static constexpr int STAT_BYTES = 2 * 256 * 4;  // per stage: -LSE*log2e[128], Delta[128]
+  static constexpr int BAR_OFF = STAT_OFF + STAT_BYTES;
+  // kv_full, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full, p_full,
+  // ds_full, ds_empty, dq_full, dq_empty, mma_done
+  static constexpr int NBAR = 15;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int SMEM_BYTES = MISC_OFF + 16;
+  // at least 117 KB, so that one CTA (which takes all of TMEM) runs per SM
+  static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024 > 119808) ? SMEM_BYTES + 1024 : 119808;
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t DV_COL = 0, DK_COL = D, S_COL = 2 * D, DP_COL = 2 * D + 128;
+  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(DP_COL + 128 <= TMEM_COLS, "tensor memory");
+  static_assert(SMEM_ALLOC <= 232448, "shared memory");
+};
+
+// The key tile of this CTA and the query tiles that see it.
+struct BwdTile {
+  int plane;
+  int q_base, q_len;    // the sequence's first query row in the maps, and its query count
+  int kv_base, kv_len;  // likewise for keys
+  int kblk;             // 128-key block within the sequence
+  int qt0, nqt;         // first query tile that sees a key of the block, and the tile count
+};
+
+// Dense layout: CTA t takes key block t / planes of plane t % planes, so the
+// blocks that see the most query tiles under the causal mask (block 0) start
+// first.  Packed layout: key blocks sequence by sequence.  Returns false when
+// the CTA has no block (or cu_seqlens is malformed).
+__device__ __forceinline__ bool bwd_tile(const BwdParams& p, BwdTile& w) {
+  const int t = static_cast<int>(blockIdx.x);
+  w.plane = t % p.planes;
+  const int vb = t / p.planes;
+  if (p.cu_seqlens == nullptr) {
+    if (vb >= p.n_kblk) return false;
+    w.kblk = vb;
+    w.q_base = 0;
+    w.q_len = p.rows;
+    w.kv_base = 0;
+    w.kv_len = p.rows_k;
+  } else {
+    int cum = 0;
+    bool found = false;
+    for (int s = 0; s < p.nseq; ++s) {
+      const int ak = __ldg(p.cu_seqlens_k + s), ek = __ldg(p.cu_seqlens_k + s + 1);
+      if (ak < 0 || ek < ak || ek > p.rows_k) {
+        if (threadIdx.x == 0) atomicOr(p.err, kDevErrBounds);
+        return false;
+      }
+      const int nb = (ek - ak + 127) / 128;
+      if (vb < cum + nb) {
+        const int a = __ldg(p.cu_seqlens + s), e = __ldg(p.cu_seqlens + s + 1);
+        if (a < 0 || e < a || e > p.rows) {
+          if (threadIdx.x == 0) atomicOr(p.err, kDevErrBounds);
+          return false;
+        }
+        w.q_base = a;
+        w.q_len = e - a;
+        w.kv_base = ak;
+        w.kv_len = ek - ak;
+        w.kblk = vb - cum;
+        found = true;
+        break;
+      }
+      cum += nb;
+    }
+    if (!found) return false;
+  }
+  const int nq_tiles = (w.q_len + 127) / 128;
+  int first = 0;
+  if (p.causal) {
+    // the first query that sees key k0 is k0 - (Nk - Nq)
+    const int r = w.kblk * 128 - (w.kv_len - w.q_len);
+    first = r <= 0 ? 0 : r / 128;
+  }
+  w.qt0 = min(first, nq_tiles);
+  w.nqt = nq_tiles - w.qt0;
+  return true;
+}
+
+// acc (+)= A B over kdim/16 steps with both operands K-major in shared memory.
+template <int KDIM>
+__device__ __forceinline__ void bwd_mma_kk(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < KDIM / 16; ++kk) {
+    const uint32_t off = ((kk / 4) * (128 * 128) + (kk % 4) * 32) >> 4;
+    umma_ss_warp(d_tmem, a + off, b + off, idesc, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D, bool F16>
+__global__ void __launch_bounds__(320, 1)
+    attn_bwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmDO, const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = bars + 1;   // [2]
+  uint64_t* q_empty = bars + 3;  // [2]
+  uint64_t* do_full = bars + 5;
+  uint64_t* do_empty = bars + 6;
+  uint64_t* s_full = bars + 7;
+  uint64_t* dp_full = bars + 8;
+  uint64_t* p_full = bars + 9;
+  uint64_t* ds_full = bars + 10;
+  uint64_t* ds_empty = bars + 11;
+  uint64_t* dq_full = bars + 12;
+  uint64_t* dq_empty = bars + 13;
+  uint64_t* mma_done = bars + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+  float* stat = reinterpret_cast<float*>(smem + C::STAT_OFF);
+
+  BwdTile w;
+  if (!bwd_tile(p, w)) return;  // uniform over the CTA
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int n = w.nqt;
+  const int k0 = w.kblk * C::BN;
+  const int off = w.kv_len - w.q_len;  // causal alignment of queries to keys
+  const size_t kv_row0 = static_cast<size_t>(w.plane) * p.rows_k + w.kv_base + k0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1 + 32);  // 32 producer lanes (LSE/Delta) + the expect_tx arrival
+      mbar_init(&q_empty[i], 1);
+    }
+    mbar_init(do_full, 1);
+    mbar_init(do_empty, 1);
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(ds_full, 128);
+    mbar_init(ds_empty, 1);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 128);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
+  const uint32_t smem_base = smem_u32(smem);
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl));
+  };
+
+  // Writes one 128-key slice (this thread's key row) of dK or dV from TMEM.
+  auto store_rows = [&](uint32_t t_src, void* dst_base, int row, float mul, bool zero) {
+    const bool valid = k0 + row < w.kv_len;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(dst_base) + (kv_row0 + row) * D);
+#pragma unroll
+    for (int cc = 0; cc < D / 32; ++cc) {
+      uint32_t r[32];
+      if (!zero) {
+        tmem_ld32_wait(t_src + 32 * cc, r);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) r[e] = 0u;
+      }
+      uint32_t h[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        h[e] = pack_16x2<F16>(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+      if (valid) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          dst[cc * 4 + v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+      }
+    }
+  };
+
+  if (n == 0) {
+    // no query sees these keys: their gradients are zero
+    if (warp < 4) {
+      store_rows(0, p.dv, threadIdx.x, 1.f, true);
+      store_rows(0, p.dk, threadIdx.x, 1.f, true);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ P and dS
+    const int t = threadIdx.x;  // key row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+    const uint32_t tS = tmem + lane_off + C::S_COL;
+    const uint32_t tDP = tmem + lane_off + C::DP_COL;
+    const int key = k0 + t;
+    const bool key_ok = key < w.kv_len;
+    const uint64_t c2 = f32x2(p.scale_log2, p.scale_log2);
+    const uint32_t ds_row = smem_base + C::DS_OFF + t * 128;
+    bool ok = true;
+    for (int i = 0; i < n && ok; ++i) {
+      const int st = i & 1;
+      const int q0 = (w.qt0 + i) * C::BM;
+      const float* nlse = stat + st * 256;  // -LSE * log2(e) per query column
+      const float* dlt = nlse + 128;        // Delta per query column
+      if (!wait(s_full, i & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld128_wait(tS, sr);
+      // columns c < cmin are future queries for this key (causal)
+      const int cmin = p.causal ? key - off - q0 : -1;
+      const bool need_mask = !key_ok || (p.causal && k0 + C::BN - 1 > q0 + off);
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const uint64_t nl = *reinterpret_cast<const uint64_t*>(nlse + 2 * c);
+        const uint64_t x2 = ffma2(u32x2(sr[2 * c], sr[2 * c + 1]), c2, nl);
+        float a = ex2_approx(lo_f32(x2));
+        float b = ex2_approx(hi_f32(x2));
+        if (need_mask) {
+          if (!key_ok || 2 * c < cmin) a = 0.f;
+          if (!key_ok || 2 * c + 1 < cmin) b = 0.f;
+        }
+        pk[c] = pack_16x2<F16>(a, b);
+      }
+      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full);
+
+      if (!wait(dp_full, i & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // the previous dS must have been read by its dK and dQ MMAs
+      if (i > 0 && !wait(ds_empty, (i - 1) & 1)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t dr[32];
+        tmem_ld32_wait(tDP + 32 * cc, dr);
+        uint32_t h[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint32_t pp = pk[16 * cc + e];
+          float plo, phi;
+          if constexpr (F16) {
+            const __half2 hv = *reinterpret_cast<const __half2*>(&pp);
+            plo = __low2float(hv);
+            phi = __high2float(hv);
+          } else {
+            plo = __uint_as_float(pp << 16);
+            phi = __uint_as_float(pp & 0xffff0000u);
+          }
+          const int col = 32 * cc + 2 * e;
+          const float a = plo * (__uint_as_float(dr[2 * e]) - dlt[col]);
+          const float b = phi * (__uint_as_float(dr[2 * e + 1]) - dlt[col + 1]);
+          h[e] = pack_16x2<F16>(a, b);
+        }
+        // 32 queries = 64 bytes = four 16-byte units of this key's 128-byte row
+        const uint32_t chunk = ds_row + (cc / 2) * C::CHUNK_BYTES;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t unit = static_cast<uint32_t>((cc % 2) * 4 + u) ^ static_cast<uint32_t>(t & 7);
+          st_shared_v4(chunk + unit * 16, h[4 * u], h[4 * u + 1], h[4 * u + 2], h[4 * u + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+    }
+    // dV epilogue
+    if (ok && wait(mma_done, 0)) {
+      tc_fence_after();
+      store_rows(tmem + lane_off + C::DV_COL, p.dv, t, 1.f, false);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ dQ drain
+    const int t = threadIdx.x - 128;  // query row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp - 4)) << 16;
+    const uint32_t tQ = tmem + lane_off + C::DP_COL;
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      if (!wait(dq_full, i & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int qrow = (w.qt0 + i) * C::BM + t;
+      const bool valid = qrow < w.q_len;
+      float* dst = p.dq_acc + (static_cast<size_t>(w.plane) * p.rows + w.q_base + qrow) * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32_wait(tQ + 32 * cc, r);
+        if (valid) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            red_add_v4(dst + 32 * cc + 4 * v, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+    }
+    // dK epilogue (dK = scale * dS^T Q)
+    if (ok && wait(mma_done, 0)) {
+      tc_fence_after();
+      store_rows(tmem + lane_off + C::DK_COL, p.dk, t, p.scale, false);
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t id_s = idesc_bf16_f32(128, 128, 0, 0, F16);  // S^T, dP^T
+    constexpr uint32_t id_kv = idesc_bf16_f32(128, D, 0, 1, F16);   // dV (TS), dK
+    constexpr uint32_t id_dq = idesc_bf16_f32(128, D, 1, 1, F16);   // dQ: A MN-major
+    const uint64_t kA = sdesc_sw128(smem_base + C::K_OFF, 16, 1024);
+    const uint64_t vA = sdesc_sw128(smem_base + C::V_OFF, 16, 1024);
+    const uint64_t kMN = sdesc_sw128(smem_base + C::K_OFF, C::CHUNK_BYTES, 1024);
+    const uint64_t doK = sdesc_sw128(smem_base + C::DO_OFF, 16, 1024);
+    const uint64_t doMN = sdesc_sw128(smem_base + C::DO_OFF, C::CHUNK_BYTES, 1024);
+    const uint64_t dsK = sdesc_sw128(smem_base + C::DS_OFF, 16, 1024);
+    const uint64_t dsMN = sdesc_sw128(smem_base + C::DS_OFF, C::CHUNK_BYTES, 1024);
+    const uint64_t qK[2] = {sdesc_sw128(smem_base + C::Q_OFF, 16, 1024),
+                            sdesc_sw128(smem_base + C::Q_OFF + C::TILE_BYTES, 16, 1024)};
+    const uint64_t qMN[2] = {sdesc_sw128(smem_base + C::Q_OFF, C::CHUNK_BYTES, 1024),
+                             sdesc_sw128(smem_base + C::Q_OFF + C::TILE_BYTES, C::CHUNK_BYTES,
+                                         1024)};
+    const uint32_t tS = tmem + C::S_COL, tDP = tmem + C::DP_COL;
+    const uint32_t tDV = tmem + C::DV_COL, tDK = tmem + C::DK_COL;
+    bool ok = wait(kv_full, 0) && wait(&q_full[0], 0);
+    if (ok) {
+      tc_fence_after();
+      bwd_mma_kk<D>(tS, kA, qK[0], id_s, 0);  // S_0^T = K Q_0^T
+      umma_commit_warp(s_full);
+    }
+    for (int i = 0; ok && i < n; ++i) {
+      const int st = i & 1;
+      // dP_i^T = V dO_i^T, into columns the previous dQ tile has left
+      if (!wait(do_full, i & 1) || (i > 0 && !wait(dq_empty, (i - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      bwd_mma_kk<D>(tDP, vA, doK, id_s, 0);
+      umma_commit_warp(dp_full);
+      // dV += P_i^T dO_i  (P^T from TMEM, 16 queries = 8 packed columns per step)
+      if (!wait(p_full, i & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        umma_ts_warp(tDV, tS + kk * 8, doMN + ((kk * 2048) >> 4), id_kv,
+                     (i > 0 || kk > 0) ? 1u : 0u);
+      umma_commit_warp(do_empty);
+      // S_{i+1}^T (its columns held P_i, read by the MMAs just issued)
+      if (i + 1 < n) {
+        if (!wait(&q_full[(i + 1) & 1], ((i + 1) >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        bwd_mma_kk<D>(tS, kA, qK[(i + 1) & 1], id_s, 0);
+        umma_commit_warp(s_full);
+      }
+      // dK += dS_i^T Q_i and dQ_i = dS_i K
+      if (!wait(ds_full, i & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = ((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
+        umma_ss_warp(tDK, dsK + aoff, qMN[st] + ((kk * 2048) >> 4), id_kv,
+                     (i > 0 || kk > 0) ? 1u : 0u);
+      }
+      umma_commit_warp(&q_empty[st]);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        umma_ss_warp(tDP, dsMN + ((kk * 2048) >> 4), kMN + ((kk * 2048) >> 4), id_dq,
+                     kk > 0 ? 1u : 0u);
+      umma_commit_warp(dq_full);
+      umma_commit_warp(ds_empty);
+    }
+    // every MMA issued must finish before TMEM and shared memory are released
+    umma_commit_warp(mma_done);
+    mbar_wait_drain(mma_done, 0, ctl);
+  } else {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+    }
+    __syncwarp();
+    const int krow = w.kv_base + k0;
+    mbar_arrive_expect_tx_warp(kv_full, 2 * C::TILE_BYTES);
+#pragma unroll
+    for (int c = 0; c < C::NCHUNK; ++c) {
+      tma_load_3d_warp(smem_base + C::K_OFF + c * C::CHUNK_BYTES, &tmK, smem_u32(kv_full), c * 64,
+                       krow, w.plane);
+      tma_load_3d_warp(smem_base + C::V_OFF + c * C::CHUNK_BYTES, &tmV, smem_u32(kv_full), c * 64,
+                       krow, w.plane);
+    }
+    int nq_issued = 0, ndo_issued = 0;
+    for (int i = 0; i < n; ++i) {
+      const int st = i & 1;
+      const int q0 = (w.qt0 + i) * C::BM;
+      if (i >= 2 && !wait(&q_empty[st], ((i >> 1) - 1) & 1)) break;
+      // this tile's LSE (as -LSE*log2e) and Delta; columns past the sequence
+      // get -inf and 0, so their P and dS are zero
+      float* sdst = stat + st * 256;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = lane * 4 + e;
+        const int q = q0 + c;
+        float nl = -INFINITY, dl = 0.f;
+        if (q < w.q_len) {
+          const size_t g = static_cast<size_t>(w.plane) * p.rows + w.q_base + q;
+          nl = -__ldg(p.lse + g) * 1.4426950408889634f;
+          dl = __ldg(p.delta + g);
+        }
+        sdst[c] = nl;
+        sdst[128 + c] = dl;
+      }
+      mbar_arrive(&q_full[st]);
+      mbar_arrive_expect_tx_warp(&q_full[st], C::TILE_BYTES);
+#pragma unroll
+      for (int c = 0; c < C::NCHUNK; ++c)
+        tma_load_3d_warp(smem_base + C::Q_OFF + st * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ,
+                         smem_u32(&q_full[st]), c * 64, w.q_base + q0, w.plane);
+      ++nq_issued;
+      if (i >= 1 && !wait(do_empty, (i - 1) & 1)) break;
+      mbar_arrive_expect_tx_warp(do_full, C::TILE_BYTES);
+#pragma unroll
+      for (int c = 0; c < C::NCHUNK; ++c)
+        tma_load_3d_warp(smem_base + C::DO_OFF + c * C::CHUNK_BYTES, &tmDO, smem_u32(do_full),
+                         c * 64, w.q_base + q0, w.plane);
+      ++ndo_issued;
+    }
+    // drain: every copy issued must land before the CTA may exit
+    mbar_wait_drain(kv_full, 0, ctl);
+    for (int i = max(0, nq_issued - 2); i < nq_issued; ++i)
+      mbar_wait_drain(&q_full[i & 1], (i >> 1) & 1, ctl);
+    if (ndo_issued > 0) mbar_wait_drain(do_full, (ndo_issued - 1) & 1, ctl);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// Delta_i = dO_i . O_i in fp32, and a zeroed dQ accumulator row; 16 threads per row.
+template <int D, bool F16>
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p, long long nrows) {
+  constexpr int EPT = D / 16;  // elements per thread (8 or 4)
+  const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long row = gid / 16;
+  const int sub = static_cast<int>(gid % 16);
+  const bool valid = row < nrows;
+  float acc = 0.f;
+  if (valid) {
+    const uint16_t* o = static_cast<const uint16_t*>(p.o) + row * D + sub * EPT;
+    const uint16_t* g = static_cast<const uint16_t*>(p.dout) + row * D + sub * EPT;
+    uint32_t ov[4], gv[4];
+    if constexpr (EPT == 8) {
+      const uint4 a = *reinterpret_cast<const uint4*>(o);
+      const uint4 b = *reinterpret_cast<const uint4*>(g);
+      ov[0] = a.x; ov[1] = a.y; ov[2] = a.z; ov[3] = a.w;
+      gv[0] = b.x; gv[1] = b.y; gv[2] = b.z; gv[3] = b.w;
+    } else {
+      const uint2 a = *reinterpret_cast<const uint2*>(o);
+      const uint2 b = *reinterpret_cast<const uint2*>(g);
+      ov[0] = a.x; ov[1] = a.y; ov[2] = 0u; ov[3] = 0u;
+      gv[0] = b.x; gv[1] = b.y; gv[2] = 0u; gv[3] = 0u;
+    }
+#pragma unroll
+    for (int e = 0; e < EPT / 2; ++e) {
+      float o0, o1, g0, g1;
+      if constexpr (F16) {
+        const __half2 ho = *reinterpret_cast<const __half2*>(&ov[e]);
+        const __half2 hg = *reinterpret_cast<const __half2*>(&gv[e]);
+        o0 = __low2float(ho); o1 = __high2float(ho);
+        g0 = __low2float(hg); g1 = __high2float(hg);
+      } else {
+        o0 = __uint_as_float(ov[e] << 16); o1 = __uint_as_float(ov[e] & 0xffff0000u);
+        g0 = __uint_as_float(gv[e] << 16); g1 = __uint_as_float(gv[e] & 0xffff0000u);
+      }
+      acc = fmaf(o0, g0, acc);
+      acc = fmaf(o1, g1, acc);
+    }
+    float4* z = reinterpret_cast<float4*>(p.dq_acc + row * D + sub * EPT);
+#pragma unroll
+    for (int e = 0; e < EPT / 4; ++e) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (valid && sub == 0) p.delta[row] = acc;
+}
+
+// dQ = scale * accumulator, rounded once; 8 elements per thread.
+template <bool F16>
+__global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const BwdParams p, long long n8) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const float4 a = reinterpret_cast<const float4*>(p.dq_acc)[2 * i];
+  const float4 b = reinterpret_cast<const float4*>(p.dq_acc)[2 * i + 1];
+  const float s = p.scale;
+  reinterpret_cast<uint4*>(p.dq)[i] =
+      make_uint4(pack_16x2<F16>(a.x * s, a.y * s), pack_16x2<F16>(a.z * s, a.w * s),
+                 pack_16x2<F16>(b.x * s, b.y * s), pack_16x2<F16>(b.z * s, b.w * s));
+}
+
+}  // namespace attn

@@ -63,7 +63,8 @@ typedef enum {
   ATTN_ERR_BOUNDS = -8,   /* (device) cu_seqlens entries outside [0, N] or decreasing   */
   ATTN_ERR_SCALE = -9,    /* scale is not a finite number > 0                           */
   ATTN_ERR_SCRATCH = -10, /* attn_decode_noalloc: the problem needs more than the built-in
-                             scratch (ATTN_NOALLOC_SCRATCH_BYTES)                        */
+                             scratch (ATTN_NOALLOC_SCRATCH_BYTES); attn_bwd: the
+                             workspace is smaller than attn_bwd_workspace_bytes()        */
   ATTN_ERR_DTYPE = -11    /* attn_fwd_cross: element type not one of attn_dtype          */
 } attn_status;
 
@@ -134,6 +135,43 @@ int attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float
 int attn_fwd_cross(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                    int H, int Nq, int Nk, int D, const int* cu_seqlens_q,
                    const int* cu_seqlens_k, int causal, float scale, int dtype, void* stream);
+
+/*
+ * Backward pass: the gradients dQ, dK, dV of the forward for an upstream
+ * gradient dO, with the probabilities rebuilt from the forward's saved
+ * log-sum-exp -- the recomputation the "Building a FlashAttention-2 forward
+ * kernel in pure NumPy" page names as the extension after the forward
+ * ("Extending It: Your Roadmap to Senior-Level").  With P_ij =
+ * exp(scale q_i.k_j - LSE_i) on the allowed keys (the mask of attn_fwd_cross):
+ *     dV = P^T dO,  dS = P * (dO V^T - Delta),  Delta_i = dO_i . O_i,
+ *     dQ = scale dS K,  dK = scale dS^T Q.
+ *   q, k, v, B, H, Nq, Nk, D, cu_seqlens_q, cu_seqlens_k, causal, scale:
+ *          as for attn_fwd_cross (the same layouts).
+ *   o, lse : the forward's outputs for these inputs (o like q, lse fp32).
+ *   dout   : dO, like q.          dq : like q.          dk, dv : like k.
+ *   dtype  : ATTN_BF16 or ATTN_F16 (D in {64, 128}); ATTN_F32 is not offered.
+ *   workspace : caller-owned device memory of attn_bwd_workspace_bytes()
+ *          bytes, 16-byte aligned (Delta and an fp32 dQ accumulator); a
+ *          smaller one returns ATTN_ERR_SCRATCH.
+ * Arithmetic: 16-bit operands, fp32 accumulation of every product; P and dS
+ * are rounded to the 16-bit type for the MMAs that take them; dQ is
+ * accumulated over key tiles in fp32 and rounded once, as are dK and dV.
+ * The order in which key tiles add into dQ is not fixed, so dQ may differ in
+ * its last bits from run to run; dK and dV do not.
+ * Packed layout: dk and dv rows outside every sequence are left untouched;
+ * dq rows outside every sequence are written as 0.  Queries that see no key
+ * get dQ = 0; keys that no query sees get dK = dV = 0.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int D,
+             const int* cu_seqlens_q, const int* cu_seqlens_k, int causal, float scale, int dtype,
+             void* workspace, unsigned long long workspace_bytes, void* stream);
+
+/*
+ * Workspace attn_bwd needs: packed != 0 for the packed layout (Nq is then the
+ * total query tokens).  The size goes to *bytes.
+ */
+int attn_bwd_workspace_bytes(int B, int H, int Nq, int D, int packed, unsigned long long* bytes);
 
 /*
  * KV-cache decode (bf16): Nq new query rows per (batch, head) attend to all Nk

@@ -42,3 +42,59 @@ def max_err(a, b):
     if np.isnan(d).any():
         return float("inf")
     return float(d.max())
+
+
+# ---------------------------------------------------------------- backward
+#
+# Error bound of the 16-bit backward, element by element (first order in the
+# unit roundoff u: 2^-8 for bf16, 2^-11 for fp16 -- half an ulp at 1).  Every
+# product the kernel feeds to the tensor cores has at most two 16-bit roundings
+# in it (P, then dS = P (dP - Delta)), the fp32 sums add nothing of that order,
+# and each gradient is rounded once at the end.  Delta is computed from the
+# forward's 16-bit O, whose error is bounded the same way.  With T = 2u:
+#   |dV err| <= T * P^T |dO| + u |dV|
+#   |dS err| <= T * |dS| + P * |Delta err|,  |Delta err| <= |dO| . (T P|V| + u |O|)
+#   |dK err| <= scale * |dS err|^T |Q| + u |dK|,   |dQ err| <= scale * |dS err| |K| + u |dQ|
+# The bound below is twice that, plus 1e-6 absolute.
+
+def bwd_bound_plane(q, k, v, do, scale, causal, unit):
+    import oracle
+    q, k, v, do = (np.asarray(a, dtype=np.float64) for a in (q, k, v, do))
+    dq, dk, dv = oracle.attention_backward_plane(q, k, v, do, scale, causal)
+    if q.shape[0] == 0 or k.shape[0] == 0:
+        z = lambda a: np.full_like(a, 1e-6)
+        return (dq, dk, dv), (z(dq), z(dk), z(dv))
+    with np.errstate(invalid="ignore"):
+        p = np.nan_to_num(oracle.softmax_probs(q, k, scale, causal))   # rows with no key: 0
+    o = p @ v
+    delta = (do * o).sum(1, keepdims=True)
+    ds = p * (do @ v.T - delta)
+    t = 2 * unit
+    d_err = (np.abs(do) * (t * (p @ np.abs(v)) + unit * np.abs(o))).sum(1, keepdims=True)
+    ds_err = t * np.abs(ds) + p * d_err
+    b_dv = t * (p.T @ np.abs(do)) + unit * np.abs(dv)
+    b_dk = scale * (ds_err.T @ np.abs(q)) + unit * np.abs(dk)
+    b_dq = scale * (ds_err @ np.abs(k)) + unit * np.abs(dq)
+    return (dq, dk, dv), (2 * b_dq + 1e-6, 2 * b_dk + 1e-6, 2 * b_dv + 1e-6)
+
+
+def run_cuda_bwd(q, k, v, do, causal, scale, cu_seqlens=None, cu_seqlens_k=None):
+    """Forward then backward on the GPU from host tensors; fp64 numpy dQ, dK, dV."""
+    import torch
+    from exact_io_aware_107_b300 import attention_backward, attention_forward, device_error
+    dq_, dk_, dv_, ddo = (t.to("cuda") for t in (q, k, v, do))
+    cu = None if cu_seqlens is None else torch.as_tensor(cu_seqlens, dtype=torch.int32).cuda()
+    cuk = None if cu_seqlens_k is None else torch.as_tensor(cu_seqlens_k, dtype=torch.int32).cuda()
+    o, lse = attention_forward(dq_, dk_, dv_, causal=causal, scale=scale, cu_seqlens=cu,
+                               cu_seqlens_k=cuk)
+    gq = torch.full_like(dq_, float("nan"))
+    gk = torch.full_like(dk_, float("nan"))
+    gv = torch.full_like(dv_, float("nan"))
+    attention_backward(dq_, dk_, dv_, o, lse, ddo, causal=causal, scale=scale, cu_seqlens=cu,
+                       cu_seqlens_k=cuk, dq=gq, dk=gk, dv=gv)
+    assert device_error() == 0
+    f = lambda t: t.float().cpu().numpy().astype(np.float64)
+    return f(gq), f(gk), f(gv)
+
+
+UNIT = {"bf16": 2.0 ** -8, "f16": 2.0 ** -11}

@@ -100,6 +100,35 @@ def test_cross_argument_errors(lib, dtype):
     assert call(Nk=0, k=None, v=None) in (B.ATTN_OK, B.ATTN_ERR_LAUNCH)
 
 
+def test_backward_argument_errors(lib):
+    def call(**kw):
+        a = dict(q=P, k=P, v=P, o=P, lse=P, do=P, dq=P, dk=P, dv=P, B=1, H=2, Nq=16, Nk=40, D=64,
+                 cq=None, ck=None, causal=1, scale=0.125, dtype=B.ATTN_BF16, ws=P, wsb=1 << 30)
+        a.update(kw)
+        return B.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"],
+                          a["dv"], a["B"], a["H"], a["Nq"], a["Nk"], a["D"], a["cq"], a["ck"],
+                          a["causal"], a["scale"], a["dtype"], a["ws"], a["wsb"], None)
+    assert call(B=0) == B.ATTN_ERR_SHAPE
+    assert call(Nk=-1) == B.ATTN_ERR_SHAPE
+    assert call(scale=0.0) == B.ATTN_ERR_SCALE
+    assert call(dtype=B.ATTN_F32) == B.ATTN_ERR_DTYPE
+    assert call(D=96) == B.ATTN_ERR_HEADDIM
+    assert call(do=None) == B.ATTN_ERR_NULL
+    assert call(dq=None) == B.ATTN_ERR_NULL
+    assert call(dk=None) == B.ATTN_ERR_NULL
+    assert call(ws=None) == B.ATTN_ERR_NULL
+    assert call(cq=P) == B.ATTN_ERR_NULL
+    assert call(dv=P + 8) == B.ATTN_ERR_ALIGN
+    assert call(ws=P + 4) == B.ATTN_ERR_ALIGN
+    rc, need = B.attn_bwd_workspace_bytes(1, 2, 16, 64, 0)
+    assert rc == B.ATTN_OK and need == 256 + 2 * 16 * 64 * 4
+    assert call(wsb=need - 1) == B.ATTN_ERR_SCRATCH
+    assert B.attn_bwd_workspace_bytes(1, 2, 16, 80, 0)[0] == B.ATTN_ERR_HEADDIM
+    assert B.attn_bwd_workspace_bytes(3, 2, 100, 128, 1)[1] == 1024 + 2 * 100 * 128 * 4
+    assert call(Nq=0, Nk=0, q=None, k=None, v=None, o=None, lse=None, do=None, dq=None,
+                dk=None, dv=None, ws=None) == B.ATTN_OK
+
+
 def test_16bit_head_dims(lib):
     for fn in (B.attn_fwd, B.attn_fwd_f16):
         for d in (32, 96, 256):
