@@ -469,7 +469,10 @@ def run_backward(args, w):
         "metric": "attention bwd TFLOPS (bf16, 2.5x forward FLOPs)", "value": tf,
         "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic", "config": workload_config(w),
+        "dtype": "bf16", "data": "synthetic",
+        "config": {**workload_config(w),
+                   "l2": "inputs larger than L2 (no flush)" if 5 * w.hbm_bytes() / 4 > 126e6
+                   else "inputs smaller than L2 (not flushed)"},
         "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": tf / peak_tf, "peak_source": f"{peak_kind} cuBLAS bf16 burst",
                      "kernel": f"attn_bwd_bf16_kernel<{w.D}> (+ prep and dQ kernels)",

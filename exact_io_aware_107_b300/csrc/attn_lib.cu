@@ -344,7 +344,7 @@ size_t bwd_workspace_bytes(long long planes, long long nq, int D) {
 template <int D, bool F16>
 void launch_bwd_kernels(unsigned grid, cudaStream_t s, const CUtensorMap& mq,
                         const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
-                        const BwdParams& p, long long qrows) {
+                        const CUtensorMap& mdq, const BwdParams& p, long long qrows) {
   if (qrows > 0) {
     const long long threads = qrows * 16;
     attn_bwd_prep_kernel<D, F16><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(
@@ -352,7 +352,7 @@ void launch_bwd_kernels(unsigned grid, cudaStream_t s, const CUtensorMap& mq,
   }
   if (grid > 0)
     attn_bwd_bf16_kernel<D, F16><<<grid, BwdCfg<D>::THREADS, BwdCfg<D>::SMEM_ALLOC, s>>>(
-        mq, mk, mv, mdo, p);
+        mq, mk, mv, mdo, mdq, p);
   if (qrows > 0) {
     const long long n8 = qrows * D / 8;
     attn_bwd_dq_kernel<F16><<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(p, n8);
@@ -404,6 +404,7 @@ int bwd_16bit(const void* q, const void* k, const void* v, const void* o, const 
     mq = mk;
     mdo = mk;
   }
+  CUtensorMap mdq = mq;
 
   BwdParams p;
   p.o = o;
@@ -413,6 +414,18 @@ int bwd_16bit(const void* q, const void* k, const void* v, const void* o, const 
   p.dq_acc = workspace ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                                   bwd_delta_bytes(qrows))
                        : nullptr;
+  if (qrows > 0) {
+    // the fp32 dQ accumulator as a 2-D tensor (D, planes * rows), 32 x 32 boxes
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(qrows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    if (g_encode(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.dq_acc, dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+      return ATTN_ERR_LAUNCH;
+  }
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
@@ -435,14 +448,14 @@ int bwd_16bit(const void* q, const void* k, const void* v, const void* o, const 
   const unsigned g = static_cast<unsigned>(grid);
   if (D == 64) {
     if (f16)
-      launch_bwd_kernels<64, true>(g, s, mq, mk, mv, mdo, p, qrows);
+      launch_bwd_kernels<64, true>(g, s, mq, mk, mv, mdo, mdq, p, qrows);
     else
-      launch_bwd_kernels<64, false>(g, s, mq, mk, mv, mdo, p, qrows);
+      launch_bwd_kernels<64, false>(g, s, mq, mk, mv, mdo, mdq, p, qrows);
   } else {
     if (f16)
-      launch_bwd_kernels<128, true>(g, s, mq, mk, mv, mdo, p, qrows);
+      launch_bwd_kernels<128, true>(g, s, mq, mk, mv, mdo, mdq, p, qrows);
     else
-      launch_bwd_kernels<128, false>(g, s, mq, mk, mv, mdo, p, qrows);
+      launch_bwd_kernels<128, false>(g, s, mq, mk, mv, mdo, mdq, p, qrows);
   }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
@@ -696,6 +709,7 @@ extern "C" int attn_get_device_error(void* stream) {
   }
   if (v & kDevErrTimeout) return ATTN_ERR_TIMEOUT;
   if (v & kDevErrBounds) return ATTN_ERR_BOUNDS;
+  if (v & kDevErrLayout) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
 }
 

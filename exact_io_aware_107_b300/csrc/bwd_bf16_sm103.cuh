@@ -29,11 +29,17 @@
 //              as 16-bit pairs for the dV MMA; dS^T = P^T (dP^T - Delta_q) is
 //              written to shared memory for the dK and dQ MMAs.
 //   warps 4-7  "dQ" warpgroup: thread t owns query row t of the dQ tile;
-//              it reads the tile from TMEM and adds it to global memory with
-//              vector fp32 reductions.  At the end it writes dK.
+//              it loads its whole row from TMEM into registers (which frees
+//              the columns for the next dP^T at once), then stages each
+//              32 x 32 block in shared memory and adds it to the fp32
+//              accumulator with a TMA reduction (whole 128-byte lines, far
+//              fewer L2 operations than per-thread atomics).  At the end it
+//              writes dK.
 //   warp  8    tcgen05 MMA issuer and TMEM owner.
 //   warp  9    TMA producer (K, V once; Q and dO per query tile; the
-//              tile's LSE and Delta into shared memory).
+//              tile's -LSE*log2(e) and -Delta into shared memory, read from
+//              global memory before the stage is free so their latency hides
+//              behind the wait).
 //
 // TMEM columns (fp32 cells, 128 lanes): dV [0, D), dK [D, 2D),
 // S^T [2D, 2D+128) (P^T overwrites its first 64 columns), dP^T
@@ -41,8 +47,11 @@
 // once the P/dS warpgroup has read dP^T.
 //
 // Shared memory: K, V (the CTA's keys), two Q stages, one dO stage, the dS
-// tile, and the per-stage LSE/Delta vectors.  Every 128 x D tile is stored as
-// TMA writes it: D/64 chunks of 128 rows x 128 bytes, 128-byte swizzled.  The
+// tile, the per-stage LSE/Delta vectors and two 4 KB dQ staging buffers per
+// dQ warp (about 226 KB: the kernel takes the dynamic shared memory base as
+// it comes, 1024-byte aligned, and refuses to run otherwise).  Every 128 x D
+// tile is stored as TMA writes it: D/64 chunks of 128 rows x 128 bytes,
+// 128-byte swizzled.  The
 // dS tile is written in the same format with keys as rows and queries along
 // the row, so the one buffer is both the K-major A operand of dK += dS^T Q
 // (M = keys) and the MN-major A operand of dQ = dS K (M = queries).
@@ -96,15 +105,17 @@ struct BwdCfg {
   static constexpr int DS_OFF = 5 * TILE_BYTES;
   static constexpr int DS_BYTES = 2 * CHUNK_BYTES;  // 128 keys x 128 queries
   static constexpr int STAT_OFF = DS_OFF + DS_BYTES;
-  static constexpr int STAT_BYTES = 2 * 256 * 4;  // per stage: -LSE*log2e[128], Delta[128]
-  static constexpr int BAR_OFF = STAT_OFF + STAT_BYTES;
+  static constexpr int STAT_BYTES = 2 * 256 * 4;  // per stage: -LSE*log2e[128], -Delta[128]
+  static constexpr int STG_OFF = STAT_OFF + STAT_BYTES;   // dQ staging: 4 warps x 2 x 4 KB
+  static constexpr int STG_BYTES = 4 * 2 * 4096;
+  static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
   // kv_full, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full, p_full,
   // ds_full, ds_empty, dq_full, dq_empty, mma_done
   static constexpr int NBAR = 15;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16;
   // at least 117 KB, so that one CTA (which takes all of TMEM) runs per SM
-  static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024 > 119808) ? SMEM_BYTES + 1024 : 119808;
+  static constexpr int SMEM_ALLOC = (SMEM_BYTES > 119808) ? SMEM_BYTES : 119808;
   static constexpr int THREADS = 320;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t DV_COL = 0, DK_COL = D, S_COL = 2 * D, DP_COL = 2 * D + 128;
@@ -193,11 +204,15 @@ __global__ void __launch_bounds__(320, 1)
     attn_bwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
-                         const __grid_constant__ CUtensorMap tmDO, const BwdParams p) {
+                         const __grid_constant__ CUtensorMap tmDO,
+                         const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled layout needs a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicOr(p.err, kDevErrLayout);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* kv_full = bars;
   uint64_t* q_full = bars + 1;   // [2]
@@ -305,7 +320,7 @@ __global__ void __launch_bounds__(320, 1)
       const int st = i & 1;
       const int q0 = (w.qt0 + i) * C::BM;
       const float* nlse = stat + st * 256;  // -LSE * log2(e) per query column
-      const float* dlt = nlse + 128;        // Delta per query column
+      const float* dlt = nlse + 128;        // -Delta per query column
       if (!wait(s_full, i & 1)) {
         ok = false;
         break;
@@ -318,16 +333,21 @@ __global__ void __launch_bounds__(320, 1)
       const bool need_mask = !key_ok || (p.causal && k0 + C::BN - 1 > q0 + off);
       uint32_t pk[64];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const uint64_t nl = *reinterpret_cast<const uint64_t*>(nlse + 2 * c);
-        const uint64_t x2 = ffma2(u32x2(sr[2 * c], sr[2 * c + 1]), c2, nl);
-        float a = ex2_approx(lo_f32(x2));
-        float b = ex2_approx(hi_f32(x2));
-        if (need_mask) {
-          if (!key_ok || 2 * c < cmin) a = 0.f;
-          if (!key_ok || 2 * c + 1 < cmin) b = 0.f;
+      for (int c4 = 0; c4 < 32; ++c4) {
+        const uint4 nl = *reinterpret_cast<const uint4*>(nlse + 4 * c4);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = 2 * c4 + h;
+          const uint64_t x2 = ffma2(u32x2(sr[2 * c], sr[2 * c + 1]), c2,
+                                    h ? u32x2(nl.z, nl.w) : u32x2(nl.x, nl.y));
+          float a = ex2_approx(lo_f32(x2));
+          float b = ex2_approx(hi_f32(x2));
+          if (need_mask) {
+            if (!key_ok || 2 * c < cmin) a = 0.f;
+            if (!key_ok || 2 * c + 1 < cmin) b = 0.f;
+          }
+          pk[c] = pack_16x2<F16>(a, b);
         }
-        pk[c] = pack_16x2<F16>(a, b);
       }
       tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
@@ -351,21 +371,27 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld32_wait(tDP + 32 * cc, dr);
         uint32_t h[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const uint32_t pp = pk[16 * cc + e];
-          float plo, phi;
-          if constexpr (F16) {
-            const __half2 hv = *reinterpret_cast<const __half2*>(&pp);
-            plo = __low2float(hv);
-            phi = __high2float(hv);
-          } else {
-            plo = __uint_as_float(pp << 16);
-            phi = __uint_as_float(pp & 0xffff0000u);
+        for (int e4 = 0; e4 < 8; ++e4) {
+          // -Delta for four query columns
+          const uint4 nd = *reinterpret_cast<const uint4*>(dlt + 32 * cc + 4 * e4);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int e = 2 * e4 + hh;
+            const uint32_t pp = pk[16 * cc + e];
+            float plo, phi;
+            if constexpr (F16) {
+              const __half2 hv = *reinterpret_cast<const __half2*>(&pp);
+              plo = __low2float(hv);
+              phi = __high2float(hv);
+            } else {
+              plo = __uint_as_float(pp << 16);
+              phi = __uint_as_float(pp & 0xffff0000u);
+            }
+            const uint64_t d2 = fadd2(u32x2(dr[2 * e], dr[2 * e + 1]),
+                                      hh ? u32x2(nd.z, nd.w) : u32x2(nd.x, nd.y));
+            const uint64_t s2 = fmul2(f32x2(plo, phi), d2);
+            h[e] = pack_16x2<F16>(lo_f32(s2), hi_f32(s2));
           }
-          const int col = 32 * cc + 2 * e;
-          const float a = plo * (__uint_as_float(dr[2 * e]) - dlt[col]);
-          const float b = phi * (__uint_as_float(dr[2 * e + 1]) - dlt[col + 1]);
-          h[e] = pack_16x2<F16>(a, b);
         }
         // 32 queries = 64 bytes = four 16-byte units of this key's 128-byte row
         const uint32_t chunk = ds_row + (cc / 2) * C::CHUNK_BYTES;
@@ -389,29 +415,48 @@ __global__ void __launch_bounds__(320, 1)
     const int t = threadIdx.x - 128;  // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp - 4)) << 16;
     const uint32_t tQ = tmem + lane_off + C::DP_COL;
+    // Rows of the tile past the sequence's end carry dQ = 0 exactly (their P
+    // and dS columns are zero), so a box that reaches into the next plane's or
+    // sequence's rows adds zeros there; rows past the whole tensor are clipped.
     bool ok = true;
+    const uint32_t stg = smem_base + C::STG_OFF + (warp - 4) * 8192 + lane * 128;
+    int nstaged = 0;
     for (int i = 0; i < n; ++i) {
       if (!wait(dq_full, i & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int qrow = (w.qt0 + i) * C::BM + t;
-      const bool valid = qrow < w.q_len;
-      float* dst = p.dq_acc + (static_cast<size_t>(w.plane) * p.rows + w.q_base + qrow) * D;
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld32_wait(tQ + 32 * cc, r);
-        if (valid) {
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            red_add_v4(dst + 32 * cc + 4 * v, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
-        }
+      const int row0 = w.plane * p.rows + w.q_base + (w.qt0 + i) * C::BM + 32 * (warp - 4);
+      uint32_t r[D];
+      if constexpr (D == 128) {
+        tmem_ld128_wait(tQ, r);
+      } else {
+        tmem_ld64_wait(tQ, *reinterpret_cast<uint32_t(*)[64]>(&r[0]));
       }
+      // the dQ columns are free for the next dP^T as soon as they are in registers
       tc_fence_before();
       mbar_arrive(dq_empty);
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        const uint32_t buf = stg + (nstaged & 1) * 4096;
+        // the reduction that last read this buffer must be done with it
+        if (lane == 0 && nstaged >= 2) bulk_wait_group_read<1>();
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          st_shared_v4(buf + ((u ^ (lane & 7)) * 16), r[32 * cc + 4 * u], r[32 * cc + 4 * u + 1],
+                       r[32 * cc + 4 * u + 2], r[32 * cc + 4 * u + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_2d(&tmDQ, buf - lane * 128, 32 * cc, row0);
+          bulk_commit_group();
+        }
+        ++nstaged;
+      }
     }
+    if (lane == 0) bulk_wait_group<0>();
     // dK epilogue (dK = scale * dS^T Q)
     if (ok && wait(mma_done, 0)) {
       tc_fence_after();
@@ -445,7 +490,8 @@ __global__ void __launch_bounds__(320, 1)
     for (int i = 0; ok && i < n; ++i) {
       const int st = i & 1;
       // dP_i^T = V dO_i^T, into columns the previous dQ tile has left
-      if (!wait(do_full, i & 1) || (i > 0 && !wait(dq_empty, (i - 1) & 1))) {
+      if (!wait(do_full, i & 1)) { ok = false; break; }
+      if (i > 0 && !wait(dq_empty, (i - 1) & 1)) {
         ok = false;
         break;
       }
@@ -518,29 +564,31 @@ __global__ void __launch_bounds__(320, 1)
     for (int i = 0; i < n; ++i) {
       const int st = i & 1;
       const int q0 = (w.qt0 + i) * C::BM;
-      if (i >= 2 && !wait(&q_empty[st], ((i >> 1) - 1) & 1)) break;
-      // this tile's LSE (as -LSE*log2e) and Delta; columns past the sequence
-      // get -inf and 0, so their P and dS are zero
-      float* sdst = stat + st * 256;
+      // this tile's LSE (as -LSE*log2e) and -Delta, fetched before the stage is
+      // free so that their latency hides behind the wait; columns past the
+      // sequence get -inf and 0, so their P and dS are zero
+      float nl[4], dl[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int c = lane * 4 + e;
-        const int q = q0 + c;
-        float nl = -INFINITY, dl = 0.f;
+        const int q = q0 + lane * 4 + e;
+        nl[e] = -INFINITY;
+        dl[e] = 0.f;
         if (q < w.q_len) {
           const size_t g = static_cast<size_t>(w.plane) * p.rows + w.q_base + q;
-          nl = -__ldg(p.lse + g) * 1.4426950408889634f;
-          dl = __ldg(p.delta + g);
+          nl[e] = -__ldg(p.lse + g) * 1.4426950408889634f;
+          dl[e] = -__ldg(p.delta + g);
         }
-        sdst[c] = nl;
-        sdst[128 + c] = dl;
       }
-      mbar_arrive(&q_full[st]);
+      if (i >= 2 && !wait(&q_empty[st], ((i >> 1) - 1) & 1)) break;
       mbar_arrive_expect_tx_warp(&q_full[st], C::TILE_BYTES);
 #pragma unroll
       for (int c = 0; c < C::NCHUNK; ++c)
         tma_load_3d_warp(smem_base + C::Q_OFF + st * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ,
                          smem_u32(&q_full[st]), c * 64, w.q_base + q0, w.plane);
+      float* sdst = stat + st * 256;
+      *reinterpret_cast<float4*>(sdst + lane * 4) = make_float4(nl[0], nl[1], nl[2], nl[3]);
+      *reinterpret_cast<float4*>(sdst + 128 + lane * 4) = make_float4(dl[0], dl[1], dl[2], dl[3]);
+      mbar_arrive(&q_full[st]);
       ++nq_issued;
       if (i >= 1 && !wait(do_empty, (i - 1) & 1)) break;
       mbar_arrive_expect_tx_warp(do_full, C::TILE_BYTES);

@@ -234,7 +234,8 @@ const char* attn_strerror(int status);
 /*
  * Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (takes precedence) or
- * ATTN_ERR_BOUNDS; ATTN_ERR_LAUNCH if the synchronisation itself failed.
+ * ATTN_ERR_BOUNDS; ATTN_ERR_LAUNCH if the synchronisation itself failed or a
+ * kernel found its shared memory base misaligned and did not run.
  */
 int attn_get_device_error(void* stream);
 
