@@ -23,26 +23,29 @@
 //                          dQ contribution to the fp32 accumulator;
 //   attn_bwd_dq_kernel     dQ = scale * accumulator, rounded once.
 //
-// CTA layout of the main kernel (320 threads):
-//   warps 0-3  "P/dS" warpgroup: thread t owns key row t (TMEM lane t).
+// CTA layout of the main kernel (448 threads):
+//   warps 0-7  "P/dS" warps: warp w owns key rows 32*(w%4).. (TMEM lanes) and
+//              the query columns 64*(w/4) .. +63 of each tile, so two warps
+//              share each SM sub-partition and hide each other's latency.
 //              P^T = 2^(S^T * scale*log2e - LSE_q*log2e) goes back into TMEM
 //              as 16-bit pairs for the dV MMA; dS^T = P^T (dP^T - Delta_q) is
 //              written to shared memory for the dK and dQ MMAs.
-//   warps 4-7  "dQ" warpgroup: thread t owns query row t of the dQ tile;
+//   warps 8-11 "dQ" warpgroup: thread t owns query row t of the dQ tile;
 //              it loads its whole row from TMEM into registers (which frees
 //              the columns for the next dP^T at once), then stages each
 //              32 x 32 block in shared memory and adds it to the fp32
 //              accumulator with a TMA reduction (whole 128-byte lines, far
 //              fewer L2 operations than per-thread atomics).  At the end it
 //              writes dK.
-//   warp  8    tcgen05 MMA issuer and TMEM owner.
-//   warp  9    TMA producer (K, V once; Q and dO per query tile; the
+//   warp  12   tcgen05 MMA issuer and TMEM owner.
+//   warp  13   TMA producer (K, V once; Q and dO per query tile; the
 //              tile's -LSE*log2(e) and -Delta into shared memory, read from
 //              global memory before the stage is free so their latency hides
 //              behind the wait).
 //
 // TMEM columns (fp32 cells, 128 lanes): dV [0, D), dK [D, 2D),
-// S^T [2D, 2D+128) (P^T overwrites its first 64 columns), dP^T
+// S^T [2D, 2D+128) (P^T for queries 0-63 overwrites its columns 0-31 and
+// for queries 64-127 its columns 64-95, each half in columns it has read), dP^T
 // [2D+128, 2D+256); each tile's dQ (lanes = queries) reuses the dP^T columns
 // once the P/dS warpgroup has read dP^T.
 //
@@ -56,7 +59,8 @@
 // the row, so the one buffer is both the K-major A operand of dK += dS^T Q
 // (M = keys) and the MN-major A operand of dQ = dS K (M = queries).
 //
-// MMA order per query tile i:  dP_i, [P_i ready] dV += P_i^T dO_i, S_{i+1},
+// MMA order per query tile i:  dP_i (two halves of 64 queries, each as soon as
+// the previous dQ has left its columns), [P_i ready] dV += P_i^T dO_i, S_{i+1},
 // [dS_i ready] dK += dS_i^T Q_i, dQ_i = dS_i K.  S_{i+1} overwrites the
 // columns P_i was read from, which the tensor pipe orders after the dV MMA.
 #pragma once
@@ -109,14 +113,14 @@ struct BwdCfg {
   static constexpr int STG_OFF = STAT_OFF + STAT_BYTES;   // dQ staging: 4 warps x 2 x 4 KB
   static constexpr int STG_BYTES = 4 * 2 * 4096;
   static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
-  // kv_full, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full, p_full,
-  // ds_full, ds_empty, dq_full, dq_empty, mma_done
-  static constexpr int NBAR = 15;
+  // kv_full, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full[2], p_full,
+  // ds_full, ds_empty, dq_full, dq_empty[2], mma_done
+  static constexpr int NBAR = 17;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16;
   // at least 117 KB, so that one CTA (which takes all of TMEM) runs per SM
   static constexpr int SMEM_ALLOC = (SMEM_BYTES > 119808) ? SMEM_BYTES : 119808;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 448;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t DV_COL = 0, DK_COL = D, S_COL = 2 * D, DP_COL = 2 * D + 128;
   static_assert(D == 64 || D == 128, "head dim");
@@ -199,8 +203,35 @@ __device__ __forceinline__ void bwd_mma_kk(uint32_t d_tmem, uint64_t a, uint64_t
   }
 }
 
+// NCOL columns of one key row of dK or dV from TMEM (scaled by mul and
+// rounded), or zeros, to global memory.
+template <int NCOL, bool F16>
+__device__ __forceinline__ void bwd_store_row(uint32_t t_src, uint16_t* dst, bool valid, float mul,
+                                              bool zero) {
+#pragma unroll
+  for (int cc = 0; cc < NCOL / 32; ++cc) {
+    uint32_t r[32];
+    if (!zero) {
+      tmem_ld32_wait(t_src + 32 * cc, r);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) r[e] = 0u;
+    }
+    uint32_t h[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      h[e] = pack_16x2<F16>(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+    if (valid) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * cc);
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        d4[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+    }
+  }
+}
+
 template <int D, bool F16>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
     attn_bwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
@@ -220,13 +251,13 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* do_full = bars + 5;
   uint64_t* do_empty = bars + 6;
   uint64_t* s_full = bars + 7;
-  uint64_t* dp_full = bars + 8;
-  uint64_t* p_full = bars + 9;
-  uint64_t* ds_full = bars + 10;
-  uint64_t* ds_empty = bars + 11;
-  uint64_t* dq_full = bars + 12;
-  uint64_t* dq_empty = bars + 13;
-  uint64_t* mma_done = bars + 14;
+  uint64_t* dp_full = bars + 8;    // [2]: query columns 0-63, 64-127
+  uint64_t* p_full = bars + 10;
+  uint64_t* ds_full = bars + 11;
+  uint64_t* ds_empty = bars + 12;
+  uint64_t* dq_full = bars + 13;
+  uint64_t* dq_empty = bars + 14;  // [2]: TMEM columns 0-63, 64-127 read
+  uint64_t* mma_done = bars + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
   float* stat = reinterpret_cast<float*>(smem + C::STAT_OFF);
@@ -250,17 +281,19 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(do_full, 1);
     mbar_init(do_empty, 1);
     mbar_init(s_full, 1);
-    mbar_init(dp_full, 1);
-    mbar_init(p_full, 128);
-    mbar_init(ds_full, 128);
+    mbar_init(&dp_full[0], 1);
+    mbar_init(&dp_full[1], 1);
+    mbar_init(p_full, 256);
+    mbar_init(ds_full, 256);
     mbar_init(ds_empty, 1);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 128);
+    mbar_init(&dq_empty[0], 128);
+    mbar_init(&dq_empty[1], 128);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 8) {
+  if (warp == 12) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -274,66 +307,47 @@ __global__ void __launch_bounds__(320, 1)
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl));
   };
 
-  // Writes one 128-key slice (this thread's key row) of dK or dV from TMEM.
-  auto store_rows = [&](uint32_t t_src, void* dst_base, int row, float mul, bool zero) {
-    const bool valid = k0 + row < w.kv_len;
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(dst_base) + (kv_row0 + row) * D);
-#pragma unroll
-    for (int cc = 0; cc < D / 32; ++cc) {
-      uint32_t r[32];
-      if (!zero) {
-        tmem_ld32_wait(t_src + 32 * cc, r);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) r[e] = 0u;
-      }
-      uint32_t h[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e)
-        h[e] = pack_16x2<F16>(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
-      if (valid) {
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-          dst[cc * 4 + v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
-      }
-    }
+  auto row_ptr = [&](void* base, int row) {
+    return static_cast<uint16_t*>(base) + (kv_row0 + row) * D;
   };
 
   if (n == 0) {
     // no query sees these keys: their gradients are zero
     if (warp < 4) {
-      store_rows(0, p.dv, threadIdx.x, 1.f, true);
-      store_rows(0, p.dk, threadIdx.x, 1.f, true);
+      const bool valid = k0 + static_cast<int>(threadIdx.x) < w.kv_len;
+      bwd_store_row<D, F16>(0, row_ptr(p.dv, threadIdx.x), valid, 1.f, true);
+      bwd_store_row<D, F16>(0, row_ptr(p.dk, threadIdx.x), valid, 1.f, true);
     }
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ P and dS
-    const int t = threadIdx.x;  // key row within the tile
-    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-    const uint32_t tS = tmem + lane_off + C::S_COL;
-    const uint32_t tDP = tmem + lane_off + C::DP_COL;
+    const int hf = warp >> 2;              // query columns 64*hf .. 64*hf+63 of each tile
+    const int t = threadIdx.x & 127;       // key row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t tS = tmem + lane_off + C::S_COL + 64 * hf;
+    const uint32_t tDP = tmem + lane_off + C::DP_COL + 64 * hf;
     const int key = k0 + t;
     const bool key_ok = key < w.kv_len;
     const uint64_t c2 = f32x2(p.scale_log2, p.scale_log2);
-    const uint32_t ds_row = smem_base + C::DS_OFF + t * 128;
+    const uint32_t ds_row = smem_base + C::DS_OFF + hf * C::CHUNK_BYTES + t * 128;
     bool ok = true;
     for (int i = 0; i < n && ok; ++i) {
       const int st = i & 1;
-      const int q0 = (w.qt0 + i) * C::BM;
-      const float* nlse = stat + st * 256;  // -LSE * log2(e) per query column
-      const float* dlt = nlse + 128;        // -Delta per query column
+      const int q0 = (w.qt0 + i) * C::BM + 64 * hf;  // first query of this half
+      const float* nlse = stat + st * 256 + 64 * hf;  // -LSE * log2(e) per query column
+      const float* dlt = nlse + 128;                  // -Delta per query column
       if (!wait(s_full, i & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sr[128];
-      tmem_ld128_wait(tS, sr);
+      uint32_t sr[64];
+      tmem_ld64_wait(tS, sr);
       // columns c < cmin are future queries for this key (causal)
       const int cmin = p.causal ? key - off - q0 : -1;
       const bool need_mask = !key_ok || (p.causal && k0 + C::BN - 1 > q0 + off);
-      uint32_t pk[64];
+      uint32_t pk[32];
 #pragma unroll
-      for (int c4 = 0; c4 < 32; ++c4) {
+      for (int c4 = 0; c4 < 16; ++c4) {
         const uint4 nl = *reinterpret_cast<const uint4*>(nlse + 4 * c4);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -349,13 +363,13 @@ __global__ void __launch_bounds__(320, 1)
           pk[c] = pack_16x2<F16>(a, b);
         }
       }
-      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      // P^T as 16-bit pairs into the first 32 of the 64 columns just read
+      tmem_st32(tS, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full);
 
-      if (!wait(dp_full, i & 1)) {
+      if (!wait(&dp_full[hf], i & 1)) {
         ok = false;
         break;
       }
@@ -366,7 +380,7 @@ __global__ void __launch_bounds__(320, 1)
         break;
       }
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t dr[32];
         tmem_ld32_wait(tDP + 32 * cc, dr);
         uint32_t h[16];
@@ -394,32 +408,32 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
         // 32 queries = 64 bytes = four 16-byte units of this key's 128-byte row
-        const uint32_t chunk = ds_row + (cc / 2) * C::CHUNK_BYTES;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint32_t unit = static_cast<uint32_t>((cc % 2) * 4 + u) ^ static_cast<uint32_t>(t & 7);
-          st_shared_v4(chunk + unit * 16, h[4 * u], h[4 * u + 1], h[4 * u + 2], h[4 * u + 3]);
+          const uint32_t unit = static_cast<uint32_t>(cc * 4 + u) ^ static_cast<uint32_t>(t & 7);
+          st_shared_v4(ds_row + unit * 16, h[4 * u], h[4 * u + 1], h[4 * u + 2], h[4 * u + 3]);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(ds_full);
     }
-    // dV epilogue
+    // dV epilogue: this warp's half of the columns
     if (ok && wait(mma_done, 0)) {
       tc_fence_after();
-      store_rows(tmem + lane_off + C::DV_COL, p.dv, t, 1.f, false);
+      bwd_store_row<D / 2, F16>(tmem + lane_off + C::DV_COL + (D / 2) * hf,
+                                row_ptr(p.dv, t) + (D / 2) * hf, key_ok, 1.f, false);
     }
-  } else if (warp < 8) {
+  } else if (warp < 12) {
     // ------------------------------------------------------------ dQ drain
-    const int t = threadIdx.x - 128;  // query row within the tile
-    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp - 4)) << 16;
+    const int t = threadIdx.x - 256;  // query row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp - 8)) << 16;
     const uint32_t tQ = tmem + lane_off + C::DP_COL;
     // Rows of the tile past the sequence's end carry dQ = 0 exactly (their P
     // and dS columns are zero), so a box that reaches into the next plane's or
     // sequence's rows adds zeros there; rows past the whole tensor are clipped.
     bool ok = true;
-    const uint32_t stg = smem_base + C::STG_OFF + (warp - 4) * 8192 + lane * 128;
+    const uint32_t stg = smem_base + C::STG_OFF + (warp - 8) * 8192 + lane * 128;
     int nstaged = 0;
     for (int i = 0; i < n; ++i) {
       if (!wait(dq_full, i & 1)) {
@@ -427,44 +441,50 @@ __global__ void __launch_bounds__(320, 1)
         break;
       }
       tc_fence_after();
-      const int row0 = w.plane * p.rows + w.q_base + (w.qt0 + i) * C::BM + 32 * (warp - 4);
-      uint32_t r[D];
-      if constexpr (D == 128) {
-        tmem_ld128_wait(tQ, r);
-      } else {
-        tmem_ld64_wait(tQ, *reinterpret_cast<uint32_t(*)[64]>(&r[0]));
-      }
-      // the dQ columns are free for the next dP^T as soon as they are in registers
-      tc_fence_before();
-      mbar_arrive(dq_empty);
+      const int row0 = w.plane * p.rows + w.q_base + (w.qt0 + i) * C::BM + 32 * (warp - 8);
+      // Two halves of 64 columns: each is released for the next dP^T half as
+      // soon as it is in registers, then staged and reduced.
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        const uint32_t buf = stg + (nstaged & 1) * 4096;
-        // the reduction that last read this buffer must be done with it
-        if (lane == 0 && nstaged >= 2) bulk_wait_group_read<1>();
-        __syncwarp();
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          st_shared_v4(buf + ((u ^ (lane & 7)) * 16), r[32 * cc + 4 * u], r[32 * cc + 4 * u + 1],
-                       r[32 * cc + 4 * u + 2], r[32 * cc + 4 * u + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_reduce_add_2d(&tmDQ, buf - lane * 128, 32 * cc, row0);
-          bulk_commit_group();
+      for (int hq = 0; hq < 2; ++hq) {
+        constexpr int NC = (D < 64) ? D : 64;  // columns per half (the second is empty at D = 64)
+        uint32_t r[64];
+        if (hq * 64 < D) {
+          tmem_ld64_wait(tQ + 64 * hq, r);
         }
-        ++nstaged;
+        tc_fence_before();
+        mbar_arrive(&dq_empty[hq]);
+        if (hq * 64 >= D) continue;
+#pragma unroll
+        for (int cc = 0; cc < NC / 32; ++cc) {
+          const uint32_t buf = stg + (nstaged & 1) * 4096;
+          // the reduction that last read this buffer must be done with it
+          if (lane == 0 && nstaged >= 2) bulk_wait_group_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            st_shared_v4(buf + ((u ^ (lane & 7)) * 16), r[32 * cc + 4 * u],
+                         r[32 * cc + 4 * u + 1], r[32 * cc + 4 * u + 2], r[32 * cc + 4 * u + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_2d(&tmDQ, buf - lane * 128, 64 * hq + 32 * cc, row0);
+            bulk_commit_group();
+          }
+          ++nstaged;
+        }
       }
     }
     if (lane == 0) bulk_wait_group<0>();
     // dK epilogue (dK = scale * dS^T Q)
     if (ok && wait(mma_done, 0)) {
       tc_fence_after();
-      store_rows(tmem + lane_off + C::DK_COL, p.dk, t, p.scale, false);
+      bwd_store_row<D, F16>(tmem + lane_off + C::DK_COL, row_ptr(p.dk, t), k0 + t < w.kv_len,
+                            p.scale, false);
     }
-  } else if (warp == 8) {
+  } else if (warp == 12) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t id_s = idesc_bf16_f32(128, 128, 0, 0, F16);  // S^T, dP^T
+    constexpr uint32_t id_s = idesc_bf16_f32(128, 128, 0, 0, F16);   // S^T
+    constexpr uint32_t id_s64 = idesc_bf16_f32(128, 64, 0, 0, F16);   // half of dP^T
     constexpr uint32_t id_kv = idesc_bf16_f32(128, D, 0, 1, F16);   // dV (TS), dK
     constexpr uint32_t id_dq = idesc_bf16_f32(128, D, 1, 1, F16);   // dQ: A MN-major
     const uint64_t kA = sdesc_sw128(smem_base + C::K_OFF, 16, 1024);
@@ -489,24 +509,32 @@ __global__ void __launch_bounds__(320, 1)
     }
     for (int i = 0; ok && i < n; ++i) {
       const int st = i & 1;
-      // dP_i^T = V dO_i^T, into columns the previous dQ tile has left
-      if (!wait(do_full, i & 1)) { ok = false; break; }
-      if (i > 0 && !wait(dq_empty, (i - 1) & 1)) {
+      // dP_i^T = V dO_i^T in two halves of 64 queries, each into columns the
+      // previous dQ tile has left
+      if (!wait(do_full, i & 1)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      bwd_mma_kk<D>(tDP, vA, doK, id_s, 0);
-      umma_commit_warp(dp_full);
+      for (int hq = 0; hq < 2; ++hq) {
+        if (i > 0 && !wait(&dq_empty[hq], (i - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        bwd_mma_kk<D>(tDP + 64 * hq, vA, doK + ((hq * 64 * 128) >> 4), id_s64, 0);
+        umma_commit_warp(&dp_full[hq]);
+      }
+      if (!ok) break;
       // dV += P_i^T dO_i  (P^T from TMEM, 16 queries = 8 packed columns per step)
       if (!wait(p_full, i & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      // queries 16kk..16kk+15: packed columns (kk/4)*64 + (kk%4)*8 of S^T
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        umma_ts_warp(tDV, tS + kk * 8, doMN + ((kk * 2048) >> 4), id_kv,
+        umma_ts_warp(tDV, tS + (kk / 4) * 64 + (kk % 4) * 8, doMN + ((kk * 2048) >> 4), id_kv,
                      (i > 0 || kk > 0) ? 1u : 0u);
       umma_commit_warp(do_empty);
       // S_{i+1}^T (its columns held P_i, read by the MMAs just issued)
@@ -607,7 +635,7 @@ __global__ void __launch_bounds__(320, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 12) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
