@@ -18,8 +18,8 @@ import math
 from . import _binding
 from ._binding import AttnError
 
-__all__ = ["attention_forward", "attention_backward", "attention_decode", "AttnError",
-           "device_error", "load_library"]
+__all__ = ["attention_forward", "attention_forward_host", "attention_backward",
+           "attention_decode", "AttnError", "device_error", "load_library"]
 
 
 def load_library():
@@ -106,6 +106,48 @@ def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens=None, out=No
         where = "attention_forward"
     if rc != _binding.ATTN_OK:
         raise AttnError(rc, where)
+    return out, lse
+
+
+def attention_forward_host(q, k, v, causal=False, scale=None, out=None, lse=None, workspace=None,
+                           stream=None, device=None):
+    """The forward on host tensors (B, H, N, D): bf16, fp16 or fp32 CPU tensors,
+    page-locked (``pin_memory()``) for the copies to overlap the compute.
+
+    Copies in, computes and copies back chunk by chunk on the current CUDA
+    device; returns (O, LSE) as host tensors once the stream has synchronised.
+    ``workspace``: a CUDA tensor of at least ``attn_fwd_host_workspace_bytes``
+    bytes (256-byte aligned), or None to let torch allocate one here.
+    """
+    import torch
+
+    kinds = {torch.bfloat16: _binding.ATTN_BF16, torch.float16: _binding.ATTN_F16,
+             torch.float32: _binding.ATTN_F32}
+    if q.dtype not in kinds or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share a dtype: bfloat16, float16 or float32")
+    for t in (q, k, v):
+        if t.is_cuda or not t.is_contiguous() or t.dim() != 4 or t.shape != q.shape:
+            raise ValueError("q, k, v must be contiguous (B, H, N, D) host tensors of one shape")
+    B, H, N, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q, pin_memory=True)
+    if lse is None:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, pin_memory=True)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    if workspace is None:
+        rc, nbytes = _binding.attn_fwd_host_workspace_bytes(B, H, N, D, kinds[q.dtype])
+        if rc != _binding.ATTN_OK:
+            raise AttnError(rc, "attention_forward_host")
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    rc = _binding.attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, D,
+                                causal, scale, kinds[q.dtype], _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), stream.cuda_stream)
+    if rc != _binding.ATTN_OK:
+        raise AttnError(rc, "attention_forward_host")
     return out, lse
 
 

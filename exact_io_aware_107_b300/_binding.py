@@ -45,6 +45,11 @@ _SIGNATURES = {
     "attn_fwd_cross": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
                        + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
                           ctypes.c_int, ctypes.c_void_p]),
+    "attn_fwd_host": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
+                      + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_ulonglong,
+                         ctypes.c_void_p]),
+    "attn_fwd_host_workspace_bytes": (ctypes.c_int, [ctypes.c_int] * 5
+                                      + [ctypes.POINTER(ctypes.c_ulonglong)]),
     "attn_bwd": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 5
                  + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int,
                     ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_void_p]),
@@ -119,6 +124,21 @@ def attn_fwd_cross(q, k, v, o, lse, B, H, Nq, Nk, D, cu_seqlens_q, cu_seqlens_k,
     return load().attn_fwd_cross(q, k, v, o, lse, int(B), int(H), int(Nq), int(Nk), int(D),
                                  cu_seqlens_q, cu_seqlens_k, int(causal), float(scale),
                                  int(dtype), stream)
+
+
+def attn_fwd_host(q, k, v, o, lse, B, H, N, D, causal, scale, dtype, workspace, workspace_bytes,
+                  stream) -> int:
+    """Forward from host buffers (q, k, v, o, lse are host addresses)."""
+    return load().attn_fwd_host(q, k, v, o, lse, int(B), int(H), int(N), int(D), int(causal),
+                                float(scale), int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def attn_fwd_host_workspace_bytes(B, H, N, D, dtype):
+    """(status, bytes) for the host-buffer forward's device workspace."""
+    n = ctypes.c_ulonglong(0)
+    rc = load().attn_fwd_host_workspace_bytes(int(B), int(H), int(N), int(D), int(dtype),
+                                              ctypes.byref(n))
+    return rc, n.value
 
 
 def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, D, cu_seqlens_q, cu_seqlens_k,

@@ -648,6 +648,156 @@ extern "C" int attn_fwd_cross(const void* q, const void* k, const void* v, void*
                  dtype, stream);
 }
 
+namespace {
+// Host-buffer forward: copies in, kernels and copies out of successive chunks
+// of planes run on three streams of their own (created once per device), so
+// that the two copy directions and the kernels overlap.
+constexpr int kHostChunks = 8;
+
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t in_ready[2] = {}, out_ready[2] = {}, slot_free[2] = {};
+  std::mutex mu;  // one call enqueues at a time on a device
+};
+HostPipe g_pipe[kMaxDevices];
+
+int host_pipe(HostPipe** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  HostPipe& hp = g_pipe[dev];
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!hp.ready) {
+    bool ok = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.comp, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < 2; ++i)
+      ok = cudaEventCreateWithFlags(&hp.in_ready[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&hp.out_ready[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&hp.slot_free[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      return ATTN_ERR_LAUNCH;
+    }
+    hp.ready = true;
+  }
+  *out = &hp;
+  return ATTN_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct HostPlan {
+  long long ppc;     // planes per chunk
+  long long nchunk;
+  size_t tile;       // bytes of one q/k/v/o chunk buffer
+  size_t lse;        // bytes of one lse chunk buffer
+  size_t slot;       // bytes of one slot (q, k, v, o, lse)
+};
+
+HostPlan host_plan(long long planes, int N, int D, size_t elt) {
+  HostPlan h;
+  const long long chunks = std::min<long long>(planes, kHostChunks);
+  h.ppc = (planes + chunks - 1) / chunks;
+  h.nchunk = (planes + h.ppc - 1) / h.ppc;
+  h.tile = round256(static_cast<size_t>(h.ppc) * N * D * elt);
+  h.lse = round256(static_cast<size_t>(h.ppc) * N * 4);
+  h.slot = 4 * h.tile + h.lse;
+  return h;
+}
+
+size_t dtype_size(int dtype) { return dtype == ATTN_F32 ? 4 : 2; }
+}  // namespace
+
+extern "C" int attn_fwd_host_workspace_bytes(int B, int H, int N, int D, int dtype,
+                                             unsigned long long* bytes) {
+  if (!bytes) return ATTN_ERR_NULL;
+  if (B < 1 || H < 1 || N < 0) return ATTN_ERR_SHAPE;
+  if (dtype != ATTN_BF16 && dtype != ATTN_F16 && dtype != ATTN_F32) return ATTN_ERR_DTYPE;
+  *bytes = N == 0 ? 0 : 2 * host_plan(1LL * B * H, N, D, dtype_size(dtype)).slot;
+  return ATTN_OK;
+}
+
+extern "C" int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int H, int N, int D, int causal, float scale, int dtype,
+                             void* workspace, unsigned long long workspace_bytes, void* stream) {
+  if (B < 1 || H < 1 || N < 0) return ATTN_ERR_SHAPE;
+  if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_SCALE;
+  if (dtype != ATTN_BF16 && dtype != ATTN_F16 && dtype != ATTN_F32) return ATTN_ERR_DTYPE;
+  if (dtype == ATTN_F32 ? (D < 1 || D > 128) : (D != 64 && D != 128)) return ATTN_ERR_HEADDIM;
+  if (N == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse || !workspace) return ATTN_ERR_NULL;
+  if (!aligned(workspace, 256)) return ATTN_ERR_ALIGN;
+  const long long planes = 1LL * B * H;
+  if (planes * N > (1LL << 40)) return ATTN_ERR_SHAPE;
+  const size_t elt = dtype_size(dtype);
+  const HostPlan hp = host_plan(planes, N, D, elt);
+  if (workspace_bytes < 2 * hp.slot) return ATTN_ERR_SCRATCH;
+  DeviceState* st = nullptr;
+  int rc = prepare_device(&st);
+  if (rc != ATTN_OK) return rc;
+  HostPipe* pp = nullptr;
+  rc = host_pipe(&pp);
+  if (rc != ATTN_OK) return rc;
+
+  std::lock_guard<std::mutex> lock(pp->mu);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool ok = cudaEventRecord(pp->start, s) == cudaSuccess &&
+            cudaStreamWaitEvent(pp->h2d, pp->start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(pp->comp, pp->start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(pp->d2h, pp->start, 0) == cudaSuccess;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  for (long long c = 0; ok && c < hp.nchunk; ++c) {
+    const int slot = static_cast<int>(c & 1);
+    const long long p0 = c * hp.ppc;
+    const long long np = std::min(hp.ppc, planes - p0);
+    const size_t in_bytes = static_cast<size_t>(np) * N * D * elt;
+    const size_t in_off = static_cast<size_t>(p0) * N * D * elt;
+    const size_t lse_bytes = static_cast<size_t>(np) * N * 4;
+    const size_t lse_off = static_cast<size_t>(p0) * N;
+    uint8_t* base = ws + slot * hp.slot;
+    uint8_t *dq = base, *dk = base + hp.tile, *dv = base + 2 * hp.tile, *dout = base + 3 * hp.tile;
+    float* dlse = reinterpret_cast<float*>(base + 4 * hp.tile);
+    // inputs of chunk c go where chunk c-2 was: wait until its outputs are read back
+    if (c >= 2) ok = cudaStreamWaitEvent(pp->h2d, pp->slot_free[slot], 0) == cudaSuccess;
+    ok = ok &&
+         cudaMemcpyAsync(dq, static_cast<const uint8_t*>(q) + in_off, in_bytes,
+                         cudaMemcpyHostToDevice, pp->h2d) == cudaSuccess &&
+         cudaMemcpyAsync(dk, static_cast<const uint8_t*>(k) + in_off, in_bytes,
+                         cudaMemcpyHostToDevice, pp->h2d) == cudaSuccess &&
+         cudaMemcpyAsync(dv, static_cast<const uint8_t*>(v) + in_off, in_bytes,
+                         cudaMemcpyHostToDevice, pp->h2d) == cudaSuccess &&
+         cudaEventRecord(pp->in_ready[slot], pp->h2d) == cudaSuccess &&
+         cudaStreamWaitEvent(pp->comp, pp->in_ready[slot], 0) == cudaSuccess;
+    if (!ok) break;
+    rc = fwd_any(dq, dk, dv, dout, dlse, 1, static_cast<int>(np), N, N, D, nullptr, nullptr,
+                 causal, scale, dtype, pp->comp);
+    if (rc != ATTN_OK) break;
+    ok = cudaEventRecord(pp->out_ready[slot], pp->comp) == cudaSuccess &&
+         cudaStreamWaitEvent(pp->d2h, pp->out_ready[slot], 0) == cudaSuccess &&
+         cudaMemcpyAsync(static_cast<uint8_t*>(o) + in_off, dout, in_bytes,
+                         cudaMemcpyDeviceToHost, pp->d2h) == cudaSuccess &&
+         cudaMemcpyAsync(lse + lse_off, dlse, lse_bytes, cudaMemcpyDeviceToHost, pp->d2h) ==
+             cudaSuccess &&
+         cudaEventRecord(pp->slot_free[slot], pp->d2h) == cudaSuccess;
+  }
+  // the caller's stream continues once the last copy back is done
+  ok = ok && cudaEventRecord(pp->done, pp->d2h) == cudaSuccess &&
+       cudaStreamWaitEvent(s, pp->done, 0) == cudaSuccess;
+  if (rc != ATTN_OK) return rc;
+  if (!ok) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  return ATTN_OK;
+}
+
 extern "C" int attn_bwd_workspace_bytes(int B, int H, int Nq, int D, int packed,
                                         unsigned long long* bytes) {
   if (!bytes) return ATTN_ERR_NULL;

@@ -137,6 +137,32 @@ int attn_fwd_cross(const void* q, const void* k, const void* v, void* o, float* 
                    const int* cu_seqlens_k, int causal, float scale, int dtype, void* stream);
 
 /*
+ * Forward from HOST buffers: attn_fwd_cross's dense self-attention (Nq = Nk =
+ * N, no offsets) on q, k, v, o (B, H, N, D) and lse (B, H, N) that live in
+ * host memory.  The planes are processed in up to 8 chunks through two
+ * device slots in `workspace`; the copies to the device, the kernels and the
+ * copies back of successive chunks run on three streams the library creates
+ * once per device, so the two copy directions and the compute overlap.  The
+ * host buffers must be page-locked (cudaHostAlloc / cudaHostRegister) for the
+ * copies to overlap; pageable memory works but serialises them.  Work is
+ * ordered after what `stream` already holds, and `stream` waits for the last
+ * copy back: synchronise `stream` before reading o and lse.  Calls on one
+ * device enqueue one at a time.  Argument checks and errors as for attn_fwd;
+ * dtype as for attn_fwd_cross; a workspace smaller than
+ * attn_fwd_host_workspace_bytes() returns ATTN_ERR_SCRATCH (it must be
+ * 256-byte aligned).  This is the call a user with data in host memory makes;
+ * the pages have no counterpart beyond their (batch, heads, seq_len, dim)
+ * problem statement.
+ */
+int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                  int N, int D, int causal, float scale, int dtype, void* workspace,
+                  unsigned long long workspace_bytes, void* stream);
+
+/* Device workspace attn_fwd_host needs (two chunk slots); the size goes to *bytes. */
+int attn_fwd_host_workspace_bytes(int B, int H, int N, int D, int dtype,
+                                  unsigned long long* bytes);
+
+/*
  * Backward pass: the gradients dQ, dK, dV of the forward for an upstream
  * gradient dO, with the probabilities rebuilt from the forward's saved
  * log-sum-exp -- the recomputation the "Building a FlashAttention-2 forward

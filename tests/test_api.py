@@ -100,6 +100,29 @@ def test_cross_argument_errors(lib, dtype):
     assert call(Nk=0, k=None, v=None) in (B.ATTN_OK, B.ATTN_ERR_LAUNCH)
 
 
+def test_host_forward_argument_errors(lib):
+    def call(**kw):
+        a = dict(q=P, k=P, v=P, o=P, lse=P, B=2, H=3, N=100, D=128, causal=1, scale=0.1,
+                 dtype=B.ATTN_BF16, ws=P, wsb=1 << 30)
+        a.update(kw)
+        return B.attn_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
+                               a["D"], a["causal"], a["scale"], a["dtype"], a["ws"], a["wsb"], None)
+    assert call(B=0) == B.ATTN_ERR_SHAPE
+    assert call(N=-1) == B.ATTN_ERR_SHAPE
+    assert call(scale=0.0) == B.ATTN_ERR_SCALE
+    assert call(dtype=7) == B.ATTN_ERR_DTYPE
+    assert call(D=96) == B.ATTN_ERR_HEADDIM
+    assert call(D=96, dtype=B.ATTN_F32) != B.ATTN_ERR_HEADDIM
+    assert call(o=None) == B.ATTN_ERR_NULL
+    assert call(ws=None) == B.ATTN_ERR_NULL
+    assert call(ws=P + 128) == B.ATTN_ERR_ALIGN
+    rc, need = B.attn_fwd_host_workspace_bytes(2, 3, 100, 128, B.ATTN_BF16)
+    # 6 planes in 6 chunks of 1: two slots of q, k, v, o (100 x 128 bf16) and lse, 256-byte rounded
+    assert rc == B.ATTN_OK and need == 2 * (4 * 25600 + 512)
+    assert call(wsb=need - 1) == B.ATTN_ERR_SCRATCH
+    assert call(N=0, q=None, k=None, v=None, o=None, lse=None, ws=None) == B.ATTN_OK
+
+
 def test_backward_argument_errors(lib):
     def call(**kw):
         a = dict(q=P, k=P, v=P, o=P, lse=P, do=P, dq=P, dk=P, dv=P, B=1, H=2, Nq=16, Nk=40, D=64,
