@@ -351,7 +351,9 @@ def run_ours(args, w):
     total_ms = t_start.elapsed_time(t_end)
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     kernel_ms = sum(launch_ms) / len(launch_ms)
-    ms_step = max_over_ranks(total_ms / args.steps, ws)
+    # with an L2 flush between launches the step is the attention call alone
+    # (the events bracket it); otherwise the whole back-to-back region
+    ms_step = max_over_ranks(kernel_ms if flush is not None else total_ms / args.steps, ws)
     flops = w.flops()
     value = ws * flops / (ms_step * 1e-3) / 1e12
 
