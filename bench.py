@@ -328,6 +328,25 @@ def run_ours(args, w):
         raise RuntimeError("device error during warm-up")
 
     # --- device-timed region (inputs resident) ---
+    # Without a flush the K steps are also captured into one CUDA graph and the
+    # graph's replay is what `value` times: the same kernels back to back, with
+    # no host launch gaps in between.
+    graph = None
+    if flush is None:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            with torch.cuda.graph(graph, stream=cap):
+                for _ in range(args.steps):
+                    attention_forward(q, k, v, causal=w.causal, scale=w.scale, cu_seqlens=cu,
+                                      out=o, lse=lse, cu_seqlens_k=cuk)
+            stream.wait_stream(cap)
+            graph.replay()
+            torch.cuda.synchronize()
+        except Exception as e:  # noqa: BLE001 - fall back to the eager region
+            print(f"[bench] graph capture failed ({e}); timing the eager launches", file=sys.stderr)
+            graph = None
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(ws)
@@ -345,6 +364,15 @@ def run_ours(args, w):
             ends[i].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
+        if graph is not None:
+            g0 = torch.cuda.Event(enable_timing=True)
+            g1 = torch.cuda.Event(enable_timing=True)
+            barrier(ws)
+            with torch.cuda.stream(stream):
+                g0.record(stream)
+                graph.replay()
+                g1.record(stream)
+            torch.cuda.synchronize()
     barrier(ws)
     if device_error() != 0:
         raise RuntimeError("device error in the timed region")
@@ -352,8 +380,14 @@ def run_ours(args, w):
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     kernel_ms = sum(launch_ms) / len(launch_ms)
     # with an L2 flush between launches the step is the attention call alone
-    # (the events bracket it); otherwise the whole back-to-back region
-    ms_step = max_over_ranks(kernel_ms if flush is not None else total_ms / args.steps, ws)
+    # (the events bracket it); otherwise the K steps of the graph replay
+    if flush is not None:
+        step_ms, timing = kernel_ms, "per-launch CUDA events, L2 flushed between launches"
+    elif graph is not None:
+        step_ms, timing = g0.elapsed_time(g1) / args.steps, "one CUDA graph of the K steps"
+    else:
+        step_ms, timing = total_ms / args.steps, "K eager launches back to back"
+    ms_step = max_over_ranks(step_ms, ws)
     flops = w.flops()
     value = ws * flops / (ms_step * 1e-3) / 1e12
 
@@ -408,8 +442,8 @@ def run_ours(args, w):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": workload_config(w),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic", "config": {**workload_config(w), "timing": timing},
         "pct_of_peak": 100.0 * value / ws / peak_tf,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": achieved / peak_tf,
@@ -437,6 +471,34 @@ def run_ours(args, w):
     return 0
 
 
+def graph_step_ms(step, steps, stream, dev):
+    """Milliseconds per step of `steps` calls of step() captured into one CUDA
+    graph and replayed (the same kernels back to back, without host launch
+    gaps); None when the capture is refused."""
+    import torch
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            for _ in range(steps):
+                step(torch.cuda.current_stream(dev))
+        stream.wait_stream(cap)
+        g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+    except Exception as e:  # noqa: BLE001 - the caller falls back to eager timing
+        print(f"[bench] graph capture failed ({e})", file=sys.stderr)
+        return None
+
+
 def run_backward(args, w):
     """Backward pass (a NEXT row): device-timed TFLOP/s, 2.5x the forward's FLOPs
     (five matrix products per tile pair instead of two)."""
@@ -462,9 +524,9 @@ def run_backward(args, w):
     assert rc == 0
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
 
-    def step():
+    def step(st=stream):
         attention_backward(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, cu_seqlens=cu,
-                           cu_seqlens_k=cuk, dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
+                           cu_seqlens_k=cuk, dq=dq, dk=dk, dv=dv, workspace=ws, stream=st)
 
     for _ in range(args.warmup):
         step()
@@ -479,9 +541,11 @@ def run_backward(args, w):
             step()
             ends[i].record(stream)
         torch.cuda.synchronize()
+        g_ms = graph_step_ms(step, args.steps, stream, dev)
     if device_error() != 0:
         raise RuntimeError("device error in the timed region")
-    ms = sum(s_.elapsed_time(e) for s_, e in zip(starts, ends)) / args.steps
+    eager_ms = sum(s_.elapsed_time(e) for s_, e in zip(starts, ends)) / args.steps
+    ms = g_ms if g_ms is not None else eager_ms
     flops = 2.5 * w.flops()
     peak_tf, _, peak_kind = load_peaks()
     tf = flops / (ms * 1e-3) / 1e12
@@ -493,7 +557,9 @@ def run_backward(args, w):
         "dtype": "bf16", "data": "synthetic",
         "config": {**workload_config(w),
                    "l2": "inputs larger than L2 (no flush)" if 5 * w.hbm_bytes() / 4 > 126e6
-                   else "inputs smaller than L2 (not flushed)"},
+                   else "inputs smaller than L2 (not flushed)",
+                   "timing": "one CUDA graph of the K steps" if g_ms is not None
+                   else "per-step CUDA events"},
         "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": tf / peak_tf, "peak_source": f"{peak_kind} cuBLAS bf16 burst",
                      "kernel": f"attn_bwd_bf16_kernel<{w.D}> (+ prep and dQ kernels)",
@@ -537,8 +603,11 @@ def run_decode(args):
             attention_decode(dq, dk, dv, workspace=ws, out=o, lse=lse, stream=stream)
         e1.record(stream)
         torch.cuda.synchronize()
+        g_ms = graph_step_ms(lambda st: attention_decode(dq, dk, dv, workspace=ws, out=o, lse=lse,
+                                                         stream=st),
+                             args.steps, stream, dev)
     assert device_error() == 0
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = g_ms if g_ms is not None else e0.elapsed_time(e1) / args.steps
     nbytes_alg = 2 * B * H * Nk * D * 2 + 2 * B * H * Nq * D * 2 + B * H * Nq * 4
     _, hbm_peak, kind = load_peaks()
     gbs = nbytes_alg / (ms * 1e-3) / 1e9
@@ -549,6 +618,8 @@ def run_decode(args):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"decode_b{B}_h{H}_nq{Nq}_nk{Nk}_d{D}", "B": B, "H": H, "Nq": Nq,
                    "Nk": Nk, "D": D, "workspace_bytes": nbytes,
+                   "timing": "one CUDA graph of the K steps" if g_ms is not None
+                   else "K launches back to back",
                    "l2": "K/V larger than L2 (no flush)" if 2 * B * H * Nk * D * 2 > 126e6
                    else "K/V fit in L2"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
