@@ -323,7 +323,8 @@ __global__ void __launch_bounds__(320, 1)
         continue;
       }
       float m_ref = -INFINITY;
-      float l = 0.f;
+      float l = 0.f;    // row sum of the probabilities (for LSE)
+      float l_o = 0.f;  // the same with each tile's largest term as rounded (for O)
       bool ok = true;
       for (int j = 0; j < n_i; ++j) {
         // warp-uniform outcome: the TMEM loads below are warp-collective
@@ -357,7 +358,8 @@ __global__ void __launch_bounds__(320, 1)
             mx[e] = fmax3(mx[e], __uint_as_float(sr[c + e]), __uint_as_float(sr[c + 4 + e]));
         const float tail = fmax3(__uint_as_float(sr[124]), __uint_as_float(sr[125]),
                                  fmaxf(__uint_as_float(sr[126]), __uint_as_float(sr[127])));
-        const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], tail) * cl2;
+        const float mraw = fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], tail);
+        const float mt = mraw * cl2;
         float m_new = m_ref;
         float alpha = 1.f;
         bool resc = false;
@@ -368,6 +370,15 @@ __global__ void __launch_bounds__(320, 1)
         }
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const uint64_t nm2 = f32x2(-m_use, -m_use);
+        // The tile's largest probability, computed exactly as the loop below
+        // computes it, and the error its rounding to 16 bits makes.  O is
+        // divided by the row sum corrected by these errors, so that the term
+        // that dominates a peaked row enters numerator and denominator alike
+        // (its P can be up to 2^8 under the lazy rescale, and a relative 2^-8
+        // on it would otherwise move O by up to 2^-8 |V|); LSE keeps the sum
+        // of the unrounded probabilities.
+        const float pmx = ex2_approx(fmaf(mraw, cl2, -m_use));
+        const float pmx_err = lo_f32(unpack_16x2<F16>(pack_16x2<F16>(pmx, 0.f))) - pmx;
         uint64_t acc2[2] = {0ull, 0ull};
         uint32_t pk[64];
 #pragma unroll
@@ -379,7 +390,9 @@ __global__ void __launch_bounds__(320, 1)
           pk[c] = pack_16x2<F16>(a, b);
         }
         const uint64_t sum2 = fadd2(acc2[0], acc2[1]);
-        l = l * alpha + (lo_f32(sum2) + hi_f32(sum2));
+        const float tile_sum = lo_f32(sum2) + hi_f32(sum2);
+        l = l * alpha + tile_sum;
+        l_o = l_o * alpha + (tile_sum + pmx_err);
         tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
         tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         if (__any_sync(0xffffffffu, resc)) {
@@ -409,7 +422,7 @@ __global__ void __launch_bounds__(320, 1)
       const bool valid = row < w.seq_len;
       const size_t grow = static_cast<size_t>(w.plane) * p.rows + w.row_base + row;
       // l == 0 only for a row that saw no allowed key: O = 0, LSE = -inf
-      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      const float inv_l = (l > 0.f) ? 1.f / l_o : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + grow * D);
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {

@@ -452,6 +452,22 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// The two 16-bit values of a packed pair, widened exactly to fp32 (as an f32x2).
+template <bool F16>
+__device__ __forceinline__ uint64_t unpack_16x2(uint32_t x);
+template <>
+__device__ __forceinline__ uint64_t unpack_16x2<false>(uint32_t x) {
+  return u32x2(x << 16, x & 0xffff0000u);
+}
+template <>
+__device__ __forceinline__ uint64_t unpack_16x2<true>(uint32_t x) {
+  float lo, hi;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi) : "r"(x));
+  return f32x2(lo, hi);
+}
+
 template <>
 __device__ __forceinline__ uint32_t pack_16x2<false>(float lo, float hi) {
   return pack_bf16x2(lo, hi);
