@@ -259,3 +259,41 @@ def test_full_parity_every_element(name):
     el = max(e[1] for e in errs)
     print(f"full parity {name}: max|dO| = {eo:.3e}, max|dLSE| = {el:.3e} over {o.size} outputs")
     assert eo <= BF16_TOL_O and el <= BF16_TOL_LSE, (name, eo, el)
+
+
+# ---------------------------------------------------------------- size limits
+#
+# One long plane (2^18 rows causal; a ragged 200003 rows non-causal) on sampled
+# rows, and many short planes (4096 of them) on every row of a subset: the
+# index arithmetic at the far end of the row and plane ranges.
+
+@pytest.mark.parametrize("N,D,causal", [(262144, 128, True), (200003, 64, False)])
+def test_long_plane_sampled(N, D, causal):
+    w = W.custom("bf16", B=1, H=1, N=N, D=D, causal=causal, seed=N % 97)
+    x = W.generate(w)
+    o, lse = run_cuda(x["q"], x["k"], x["v"], causal, w.scale)
+    assert not np.isnan(o).any() and not np.isnan(lse).any()
+    rows = _sample_rows(N, np.random.default_rng(5), extra=48)
+    rows = np.union1d(rows, np.arange(N - 130, N))  # the whole last tile and its edge
+    q, k, v = (W.as_f64(t[0, 0]) for t in (x["q"], x["k"], x["v"]))
+    ro, rl = oracle.attention_rows(q, k, v, w.scale, causal, rows)
+    eo, el = max_err(o[0, 0][rows], ro), max_err(lse[0, 0][rows], rl)
+    assert eo <= BF16_TOL_O and el <= BF16_TOL_LSE, (N, eo, el)
+    if causal:
+        np.testing.assert_array_equal(o[0, 0, 0], v[0])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_planes(causal):
+    B, H, N, D = 64, 64, 80, 128
+    w = W.custom("bf16", B=B, H=H, N=N, D=D, causal=causal, seed=17)
+    x = W.generate(w)
+    o, lse = run_cuda(x["q"], x["k"], x["v"], causal, w.scale)
+    rng = np.random.default_rng(6)
+    picks = {(0, 0), (B - 1, H - 1), (B - 1, 0), (0, H - 1)}
+    picks |= {(int(b), int(h)) for b, h in zip(rng.integers(0, B, 12), rng.integers(0, H, 12))}
+    for b, h in sorted(picks):
+        ro, rl = oracle.attention_plane(W.as_f64(x["q"][b, h]), W.as_f64(x["k"][b, h]),
+                                        W.as_f64(x["v"][b, h]), w.scale, causal)
+        eo, el = max_err(o[b, h], ro), max_err(lse[b, h], rl)
+        assert eo <= BF16_TOL_O and el <= BF16_TOL_LSE, (b, h, eo, el)
