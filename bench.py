@@ -161,6 +161,27 @@ class ClockSampler:
                 "samples": len(self.samples), "source": self.source}
 
 
+def system_info(dev) -> dict:
+    """The device and software the line was measured on."""
+    import torch
+    prop = torch.cuda.get_device_properties(dev)
+    info = {"sms": prop.multi_processor_count, "cc": f"{prop.major}.{prop.minor}",
+            "torch": torch.__version__, "cuda_runtime": torch.version.cuda}
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader",
+                              "-i", str(torch.cuda.current_device())],
+                             capture_output=True, text=True, timeout=20).stdout.strip()
+        info["driver"] = out.splitlines()[0] if out else None
+    except (OSError, subprocess.SubprocessError):
+        info["driver"] = None
+    try:
+        from exact_io_aware_107_b300 import _binding
+        info["library_version"] = int(_binding.attn_version())
+    except Exception:  # noqa: BLE001 - informational only
+        info["library_version"] = None
+    return info
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -460,7 +481,8 @@ def run_ours(args, w):
                      if peak_kind == "measured" else "fallback 1.8 PFLOP/s",
                      "kernel": f"attn_fwd_bf16_kernel<{w.D}>",
                      "traffic": measured_traffic(w.name),
-                     "algorithmic_bytes": w.hbm_bytes()},
+                     "algorithmic_bytes": w.hbm_bytes(),
+                     "algorithmic_gbs": w.hbm_bytes() / (kernel_ms * 1e-3) / 1e9},
         "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "call": "attn_fwd_host (pinned host buffers; chunked copies overlapped with the "
@@ -469,6 +491,7 @@ def run_ours(args, w):
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
         "gpu": torch.cuda.get_device_name(dev),
+        "system": system_info(dev),
     }
     if warm is not None:
         line["warm_l2"] = warm
@@ -577,6 +600,7 @@ def run_backward(args, w):
                      "traffic": None},
         "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
+        "gpu": torch.cuda.get_device_name(dev), "system": system_info(dev),
     }
     print(json.dumps(line))
     return 0
@@ -639,6 +663,7 @@ def run_decode(args):
                      "algorithmic_bytes": nbytes_alg},
         "gpu_launches": args.steps * (2 if nbytes > 0 else 1),
         "clocks": clk.summary(),
+        "gpu": torch.cuda.get_device_name(dev), "system": system_info(dev),
     }
     print(json.dumps(line))
     return 0
