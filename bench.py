@@ -437,7 +437,7 @@ def run_ours(args, w):
 
         def e2e_step():
             attention_forward_host(hq, hk, hv, causal=w.causal, scale=w.scale, out=ho, lse=hl,
-                                   workspace=hws, stream=stream)
+                                   workspace=hws, stream=stream, non_blocking=True)
     else:
         def e2e_step():
             q.copy_(hq, non_blocking=True)

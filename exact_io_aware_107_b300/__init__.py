@@ -110,12 +110,17 @@ def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens=None, out=No
 
 
 def attention_forward_host(q, k, v, causal=False, scale=None, out=None, lse=None, workspace=None,
-                           stream=None, device=None):
+                           stream=None, device=None, non_blocking=False):
     """The forward on host tensors (B, H, N, D): bf16, fp16 or fp32 CPU tensors,
     page-locked (``pin_memory()``) for the copies to overlap the compute.
 
     Copies in, computes and copies back chunk by chunk on the current CUDA
-    device; returns (O, LSE) as host tensors once the stream has synchronised.
+    device, ordered after the work already on ``stream`` (default: torch's
+    current stream).  By default the call returns once O and LSE are in the
+    returned host tensors (it synchronises ``stream``).  With
+    ``non_blocking=True`` it only enqueues the work, like the C call: the host
+    tensors hold the result once ``stream`` has synchronised, and the inputs
+    must not change before then.
     ``workspace``: a CUDA tensor of at least ``attn_fwd_host_workspace_bytes``
     bytes (256-byte aligned), or None to let torch allocate one here.
     """
@@ -148,6 +153,12 @@ def attention_forward_host(q, k, v, causal=False, scale=None, out=None, lse=None
                                 workspace.numel() * workspace.element_size(), stream.cuda_stream)
     if rc != _binding.ATTN_OK:
         raise AttnError(rc, "attention_forward_host")
+    if non_blocking:
+        # the library's copy and compute streams use the workspace until
+        # ``stream`` has passed the call: keep torch from handing it out before
+        workspace.record_stream(stream)
+    else:
+        stream.synchronize()
     return out, lse
 
 

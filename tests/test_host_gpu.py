@@ -54,9 +54,10 @@ def test_host_orders_after_and_before_the_callers_stream():
     hq, hk, hv = (t.pin_memory() for t in (x["q"], x["k"], x["v"]))
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
-        o1, l1 = attention_forward_host(hq, hk, hv, causal=True, scale=w.scale)
+        o1, l1 = attention_forward_host(hq, hk, hv, causal=True, scale=w.scale, non_blocking=True)
         hq2 = (hq.float() * 0.5).to(hq.dtype).pin_memory()
-        o2, l2 = attention_forward_host(hq2, hk, hv, causal=True, scale=w.scale)
+        o2, l2 = attention_forward_host(hq2, hk, hv, causal=True, scale=w.scale,
+                                        non_blocking=True)
         done = torch.cuda.Event()
         done.record(s)
     done.synchronize()
