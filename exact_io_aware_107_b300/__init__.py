@@ -30,6 +30,16 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+def _keep_for(stream, device, tensors):
+    """Tensors this module allocated on torch's current stream but handed to
+    work on another ``stream``: tell torch's allocator not to reuse their
+    memory before that work is done."""
+    import torch
+    if stream != torch.cuda.current_stream(device):
+        for t in tensors:
+            t.record_stream(stream)
+
+
 def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens=None, out=None, lse=None,
                       stream=None, cu_seqlens_k=None):
     """O and LSE of softmax(scale * Q K^T + causal mask) V.
@@ -81,12 +91,16 @@ def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens=None, out=No
     cross = Nk != N or cu_k is not None
     if scale is None:
         scale = 1.0 / math.sqrt(D)
+    own = []
     if out is None:
         out = torch.empty_like(q)
+        own.append(out)
     if lse is None:
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+        own.append(lse)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
+    _keep_for(stream, q.device, own)
     handle = stream.cuda_stream
     kinds = {torch.bfloat16: (_binding.attn_fwd, _binding.ATTN_BF16),
              torch.float16: (_binding.attn_fwd_f16, _binding.ATTN_F16),
@@ -202,16 +216,25 @@ def attention_backward(q, k, v, o, lse, dout, causal=False, scale=None, cu_seqle
             cu_k = cu_q
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    own = []
+    if dq is None:
+        dq = torch.empty_like(q)
+        own.append(dq)
+    if dk is None:
+        dk = torch.empty_like(k)
+        own.append(dk)
+    if dv is None:
+        dv = torch.empty_like(v)
+        own.append(dv)
     if workspace is None:
         rc, nbytes = _binding.attn_bwd_workspace_bytes(B, H, N, D, cu_q is not None)
         if rc != _binding.ATTN_OK:
             raise AttnError(rc, "attention_backward")
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+        own.append(workspace)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
+    _keep_for(stream, q.device, own)
     dtype = _binding.ATTN_BF16 if q.dtype == torch.bfloat16 else _binding.ATTN_F16
     rc = _binding.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                            _ptr(dk), _ptr(dv), B, H, N, Nk, D, _ptr(cu_q), _ptr(cu_k), causal,
@@ -240,17 +263,22 @@ def attention_decode(q, k, v, scale=None, workspace=None, out=None, lse=None, st
         raise ValueError("k, v must be (B, H, Nk, D) with q's B, H, D")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
+    own = []
     if out is None:
         out = torch.empty_like(q)
+        own.append(out)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+        own.append(lse)
     if workspace is None:
         rc, nbytes = _binding.attn_decode_workspace_bytes(B, H, Nq, Nk, D)
         if rc != _binding.ATTN_OK:
             raise AttnError(rc, "attention_decode")
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+        own.append(workspace)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
+    _keep_for(stream, q.device, own)
     rc = _binding.attn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, D,
                               scale, _ptr(workspace), workspace.numel() * workspace.element_size(),
                               stream.cuda_stream)

@@ -138,3 +138,65 @@ def test_concurrent_host_buffer_calls():
     for i, outs in enumerate(results):
         for o, lse in outs:
             assert torch.equal(o, ref[i][0]) and torch.equal(lse, ref[i][1])
+
+
+def test_explicit_stream_keeps_the_workspace_until_the_work_is_done():
+    # The wrappers allocate their workspace on torch's current stream.  When
+    # the work goes to another stream that is still busy, that memory must not
+    # be handed out again on the current stream when the call returns: a
+    # same-size allocation made right after the call gets other memory.
+    import torch
+    from exact_io_aware_107_b300 import attention_backward, attention_decode, attention_forward
+    from exact_io_aware_107_b300 import device_error
+    w = W.custom("bf16", B=2, H=8, N=2048, D=128, causal=True, seed=71)
+    x = W.generate(w)
+    q, k, v = (t.cuda() for t in (x["q"], x["k"], x["v"]))
+    do = W.generate(W.custom("bf16", B=2, H=8, N=2048, D=128, seed=72))["q"].cuda()
+    o, lse = attention_forward(q, k, v, causal=True)
+    ref = attention_backward(q, k, v, o, lse, do, causal=True)
+    kv = W.generate(W.custom("bf16", B=2, H=8, N=65536, D=128, seed=73))
+    kc, vc = kv["k"].cuda(), kv["v"].cuda()
+    qd = q[:, :, :2].contiguous()      # inputs stay alive until the work is done
+    ref_dec = attention_decode(qd, kc, vc)
+    torch.cuda.synchronize()
+    big = torch.zeros(1 << 28, dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+
+    def call_and_spy(fn):
+        # the byte-typed workspace the wrapper allocates: its address and size
+        seen = []
+        orig = torch.empty
+
+        def spy(*a, **kw):
+            t = orig(*a, **kw)
+            if kw.get("dtype") == torch.uint8 and t.is_cuda:
+                seen.append((t.data_ptr(), t.numel()))
+            return t
+
+        torch.empty = spy
+        try:
+            res = fn()
+        finally:
+            torch.empty = orig
+        assert len(seen) == 1
+        return res, seen[0]
+
+    for _ in range(2):
+        with torch.cuda.stream(s):
+            for _ in range(8):        # keep s busy well past the checks below
+                big.add_(1.0)
+        got, (ptr, n) = call_and_spy(
+            lambda: attention_backward(q, k, v, o, lse, do, causal=True, stream=s))
+        junk = torch.full((n,), 0x7f, dtype=torch.uint8, device="cuda")
+        assert junk.data_ptr() != ptr
+        got_dec, (ptr2, n2) = call_and_spy(lambda: attention_decode(qd, kc, vc, stream=s))
+        junk2 = torch.full((n2,), 0x7f, dtype=torch.uint8, device="cuda")
+        assert junk2.data_ptr() != ptr2
+        s.synchronize()
+        torch.cuda.synchronize()
+        del junk, junk2
+        assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+        assert torch.allclose(got[0].float(), ref[0].float(), rtol=2e-2, atol=2e-3)
+        assert torch.equal(got_dec[0], ref_dec[0]) and torch.equal(got_dec[1], ref_dec[1])
+    assert device_error() == 0
