@@ -91,7 +91,9 @@ def attention_forward(q, k, v, causal=False, scale=None, cu_seqlens=None, out=No
     cross = Nk != N or cu_k is not None
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    own = []
+    # offsets copied by .contiguous() above belong to this call too
+    own = [c for c, orig in ((cu_q, cu_seqlens), (cu_k, cu_seqlens_k))
+           if c is not None and c is not orig]
     if out is None:
         out = torch.empty_like(q)
         own.append(out)
@@ -216,7 +218,9 @@ def attention_backward(q, k, v, o, lse, dout, causal=False, scale=None, cu_seqle
             cu_k = cu_q
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    own = []
+    # offsets copied by .contiguous() above belong to this call too
+    own = [c for c, orig in ((cu_q, cu_seqlens), (cu_k, cu_seqlens_k))
+           if c is not None and c is not orig]
     if dq is None:
         dq = torch.empty_like(q)
         own.append(dq)
