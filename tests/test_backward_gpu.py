@@ -159,3 +159,31 @@ def test_backward_bf16_causal_b2_h32_n8192_d128_one_plane():
     for b, h in ((0, 0), (1, 31)):
         _check_plane((dq[b, h], dk[b, h], dv[b, h]), f(x["q"][b, h]), f(x["k"][b, h]),
                      f(x["v"][b, h]), f(do[b, h]), w.scale, True, UNIT["bf16"], (b, h))
+
+
+def test_backward_long_plane_tail_and_sampled_rows():
+    # One causal plane of 2^16 rows.  The full fp64 gradient is out of reach,
+    # but two parts of it are exact on slices: the last 256 query rows are the
+    # only ones that see the last 256 keys, so the oracle on those rows (the
+    # cross alignment: last query with last key) gives dQ of those rows and
+    # dK, dV of those keys completely; and row r's dQ needs only keys 0..r.
+    n, d = 1 << 16, 128
+    w = W.custom("bf16", B=1, H=1, N=n, D=d, causal=True, seed=15)
+    x = W.generate(w)
+    do = _dout(w, 16)
+    dq, dk, dv = run_cuda_bwd(x["q"], x["k"], x["v"], do, True, w.scale)
+    assert np.isfinite(dq).all() and np.isfinite(dk).all() and np.isfinite(dv).all()
+    q, k, v, g = (W.as_f64(t[0, 0]) for t in (x["q"], x["k"], x["v"], do))
+    u = UNIT["bf16"]
+    tail = 256
+    (rq, rk, rv), (bq, bk, bv) = bwd_bound_plane(q[n - tail:], k, v, g[n - tail:], w.scale,
+                                                 True, u)
+    assert (np.abs(dq[0, 0, n - tail:] - rq) <= bq).all()
+    assert (np.abs(dk[0, 0, n - tail:] - rk[n - tail:]) <= bk[n - tail:]).all()
+    assert (np.abs(dv[0, 0, n - tail:] - rv[n - tail:]) <= bv[n - tail:]).all()
+    rng = np.random.default_rng(16)
+    for r in sorted({0, 1, 127, 128, 129, n // 2, n - tail - 1} | set(rng.integers(0, n, 8))):
+        r = int(r)
+        (rq1, _, _), (bq1, _, _) = bwd_bound_plane(q[r:r + 1], k[:r + 1], v[:r + 1], g[r:r + 1],
+                                                   w.scale, True, u)
+        assert (np.abs(dq[0, 0, r] - rq1[0]) <= bq1[0]).all(), r
