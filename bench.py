@@ -260,10 +260,14 @@ def cpu_baseline(w, x, budget_s: float = 12.0):
         t_total += dt
         rows_done += len(rows)
         n_rows = min(4096, n_rows * 2)
+    # the same oracle on one core, on the last 256 rows
+    one = np.arange(max(0, w.N - 256), w.N)
+    f1, dt1 = oracle_rows_sample(w, x, 0, one, 1)
     return {"value": flops_total / t_total / 1e12, "unit": "TFLOP/s", "cores": threads,
-            "kind": "oracle",
+            "kind": "oracle", "value_1core": f1 / dt1 / 1e12,
             "sample": f"fp64 oracle on the last {rows_done} query rows of plane (b=0,h=0) "
-                      f"of {w.name} ({t_total:.1f} s of CPU work, {threads} threads)"}
+                      f"of {w.name} ({t_total:.1f} s of CPU work, {threads} threads); "
+                      f"value_1core: the last {len(one)} rows on one thread ({dt1:.2f} s)"}
 
 
 def run_reference(args, w):
