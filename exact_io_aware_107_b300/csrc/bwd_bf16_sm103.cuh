@@ -46,8 +46,9 @@
 // TMEM columns (fp32 cells, 128 lanes): dV [0, D), dK [D, 2D),
 // S^T [2D, 2D+128) (P^T for queries 0-63 overwrites its columns 0-31 and
 // for queries 64-127 its columns 64-95, each half in columns it has read), dP^T
-// [2D+128, 2D+256); each tile's dQ (lanes = queries) reuses the dP^T columns
-// once the P/dS warpgroup has read dP^T.
+// [2D+128, 2D+256) (dS^T as 16-bit pairs overwrites the same columns of it,
+// the A operand of dK += dS^T Q); each tile's dQ (lanes = queries) reuses the
+// dP^T columns after that dK MMA.
 //
 // Shared memory: K, V (the CTA's keys), two Q stages, one dO stage, the dS
 // tile, the per-stage LSE/Delta vectors and two 4 KB dQ staging buffers per
@@ -56,13 +57,15 @@
 // tile is stored as TMA writes it: D/64 chunks of 128 rows x 128 bytes,
 // 128-byte swizzled.  The
 // dS tile is written in the same format with keys as rows and queries along
-// the row, so the one buffer is both the K-major A operand of dK += dS^T Q
-// (M = keys) and the MN-major A operand of dQ = dS K (M = queries).
+// the row: the MN-major A operand of dQ = dS K (M = queries).  dK += dS^T Q
+// (M = keys) takes dS^T from TMEM instead, which saves the tile's second read
+// from shared memory, the resource that bounds this kernel.
 //
 // MMA order per query tile i:  dP_i (two halves of 64 queries, each as soon as
 // the previous dQ has left its columns), [P_i ready] dV += P_i^T dO_i, S_{i+1},
 // [dS_i ready] dK += dS_i^T Q_i, dQ_i = dS_i K.  S_{i+1} overwrites the
-// columns P_i was read from, which the tensor pipe orders after the dV MMA.
+// columns P_i was read from, and dQ_i the columns dS_i^T was read from, which
+// the tensor pipe orders after the MMAs that read them.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -70,6 +73,18 @@
 #include "ptx.cuh"
 
 namespace attn {
+
+// 32 lanes x 16 columns of TMEM from 16 registers per thread (asynchronous;
+// pair with tmem_wait_st).  Only the backward stores 16-column slices.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
 
 struct BwdParams {
   const void* o;            // forward output, layout of q (prep kernel)
@@ -407,6 +422,9 @@ __global__ void __launch_bounds__(448, 1)
             h[e] = pack_16x2<F16>(lo_f32(s2), hi_f32(s2));
           }
         }
+        // dS^T as 16-bit pairs into this half's dP^T columns already read
+        // (the A operand of dK += dS^T Q)
+        tmem_st16(tDP + 16 * cc, h);
         // 32 queries = 64 bytes = four 16-byte units of this key's 128-byte row
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -415,6 +433,7 @@ __global__ void __launch_bounds__(448, 1)
         }
       }
       fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(ds_full);
     }
@@ -492,7 +511,6 @@ __global__ void __launch_bounds__(448, 1)
     const uint64_t kMN = sdesc_sw128(smem_base + C::K_OFF, C::CHUNK_BYTES, 1024);
     const uint64_t doK = sdesc_sw128(smem_base + C::DO_OFF, 16, 1024);
     const uint64_t doMN = sdesc_sw128(smem_base + C::DO_OFF, C::CHUNK_BYTES, 1024);
-    const uint64_t dsK = sdesc_sw128(smem_base + C::DS_OFF, 16, 1024);
     const uint64_t dsMN = sdesc_sw128(smem_base + C::DS_OFF, C::CHUNK_BYTES, 1024);
     const uint64_t qK[2] = {sdesc_sw128(smem_base + C::Q_OFF, 16, 1024),
                             sdesc_sw128(smem_base + C::Q_OFF + C::TILE_BYTES, 16, 1024)};
@@ -553,12 +571,12 @@ __global__ void __launch_bounds__(448, 1)
         break;
       }
       tc_fence_after();
+      // dS^T from TMEM: queries 16kk..16kk+15 are packed columns
+      // (kk/4)*64 + (kk%4)*8 of the dP^T region
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t aoff = ((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
-        umma_ss_warp(tDK, dsK + aoff, qMN[st] + ((kk * 2048) >> 4), id_kv,
+      for (int kk = 0; kk < 8; ++kk)
+        umma_ts_warp(tDK, tDP + (kk / 4) * 64 + (kk % 4) * 8, qMN[st] + ((kk * 2048) >> 4), id_kv,
                      (i > 0 || kk > 0) ? 1u : 0u);
-      }
       umma_commit_warp(&q_empty[st]);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
