@@ -297,3 +297,24 @@ def test_many_planes(causal):
                                         W.as_f64(x["v"][b, h]), w.scale, causal)
         eo, el = max_err(o[b, h], ro), max_err(lse[b, h], rl)
         assert eo <= BF16_TOL_O and el <= BF16_TOL_LSE, (b, h, eo, el)
+
+
+# ---------------------------------------------------------------- scale extremes
+#
+# A tiny scale makes every row nearly uniform (LSE -> ln of the key count); a
+# large one makes rows one-hot, with most exponentials underflowing to zero and
+# a new row maximum far above the old one in many tiles.  Both are compared with
+# the oracle on every element.
+
+@pytest.mark.parametrize("scale", [1e-3, 2.0])
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("bf16", 64), ("f16", 128), ("f32", 64)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_extreme_scales(scale, dtype, D, causal):
+    w = W.custom(dtype, B=1, H=2, N=700, D=D, causal=causal, seed=23)
+    x = W.generate(w)
+    o, lse = run_cuda(x["q"], x["k"], x["v"], causal, scale)
+    ro, rl = oracle.attention(W.as_f64(x["q"]), W.as_f64(x["k"]), W.as_f64(x["v"]), scale, causal)
+    tol_o, tol_l = {"bf16": (BF16_TOL_O, BF16_TOL_LSE), "f16": (F16_TOL_O, F16_TOL_LSE),
+                    "f32": (F32_TOL_O, F32_TOL_LSE)}[dtype]
+    eo, el = max_err(o, ro), max_err(lse, rl)
+    assert eo <= tol_o and el <= tol_l, (scale, dtype, D, causal, eo, el)
