@@ -62,10 +62,6 @@ void launch_decode_kernel(unsigned grid, cudaStream_t s, const CUtensorMap& mk,
   constexpr int T = DecCfg<D>::THREADS, SM = DecCfg<D>::SMEM_ALLOC;
   if (p.nq <= 1)
     attn_decode_bf16_kernel<D, 1><<<grid, T, SM, s>>>(mk, mv, p);
-  else if (p.nq <= 2)
-    attn_decode_bf16_kernel<D, 2><<<grid, T, SM, s>>>(mk, mv, p);
-  else if (p.nq <= 4)
-    attn_decode_bf16_kernel<D, 4><<<grid, T, SM, s>>>(mk, mv, p);
   else
     attn_decode_bf16_kernel<D, 8><<<grid, T, SM, s>>>(mk, mv, p);
 }
@@ -131,9 +127,8 @@ int prepare_device(DeviceState** out) {
       cudaGetLastError();
       return ATTN_ERR_LAUNCH;
     }
-    if (set_decode_smem<64, 1>() || set_decode_smem<64, 2>() || set_decode_smem<64, 4>() ||
-        set_decode_smem<64, 8>() || set_decode_smem<128, 1>() || set_decode_smem<128, 2>() ||
-        set_decode_smem<128, 4>() || set_decode_smem<128, 8>()) {
+    if (set_decode_smem<64, 1>() || set_decode_smem<64, 8>() || set_decode_smem<128, 1>() ||
+        set_decode_smem<128, 8>()) {
       cudaGetLastError();
       return ATTN_ERR_LAUNCH;
     }

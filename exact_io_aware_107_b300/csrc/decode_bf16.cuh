@@ -15,11 +15,16 @@
 //
 // CTA: 8 compute warps in two groups that take alternate 128-key tiles, plus
 // one TMA producer warp.  Keys arrive in the forward kernel's swizzled tile
-// layout; warp w of a group scores keys 32w..32w+31 of its tile (lane = key,
-// so the row reads of the 32 lanes hit distinct banks thanks to the swizzle),
-// keeps its own running max / sum / output for the query rows, and the eight
-// warps are merged at the end.  For P.V, lane l accumulates output columns
-// [D/32 * l, D/32 * (l+1)).
+// layout; warp w of a group works on keys 32w..32w+31 of its tile, keeps its
+// own running max / sums / output for the query rows, and the eight warps are
+// merged at the end.  One query row (NQ = 1) runs on CUDA cores: lane = key
+// for the scores (the row reads of the 32 lanes hit distinct banks thanks to
+// the swizzle), and for P.V lane l accumulates output columns
+// [D/32 * l, D/32 * (l+1)).  Two to eight rows (NQ = 8) run as warp-level
+// MMAs with the rows as the M dimension (decode_rows_mma): on CUDA cores the
+// work per key grows with the rows and, from two rows on, outweighs the HBM
+// read of the key.  There P is rounded to bf16 for P.V, and O is divided by
+// the sum of the rounded weights (LSE keeps the fp32 sum).
 #pragma once
 
 #include "ptx.cuh"
@@ -59,9 +64,9 @@ struct DecCfg {
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM_ALLOC = MISC_OFF + 16 + 1024;
   // after the key loop the merge arrays reuse the (drained) K/V stages:
-  // m, l: float [8][MAXQ]; o: float [8][MAXQ][D]
+  // m, l, l_o: float [8][MAXQ]; o: float [8][MAXQ][D]
   static constexpr int M_OFF = 0;
-  static constexpr int O_OFF = 2 * 8 * kDecodeMaxQ * 4;
+  static constexpr int O_OFF = 3 * 8 * kDecodeMaxQ * 4;
   static constexpr int WARPS = 8;                                 // compute warps
   static constexpr int THREADS = 32 * WARPS + 32;
   static constexpr int CPL = D / 32;                             // output columns per lane
@@ -72,7 +77,183 @@ struct DecCfg {
 __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
-// NQ: query-row bucket (1, 2, 4 or 8); rows nq..NQ-1 of the bucket are idle.
+// ---- warp-level tensor-core helpers for the 2..8-row path
+// Four 8x8 16-bit matrices from shared memory; lane L gives the address of row
+// L % 8 of matrix L / 8 and receives (row L / 4, columns 2(L % 4), 2(L % 4)+1)
+// of each matrix (with .trans: rows 2(L % 4), 2(L % 4)+1 of column L / 4).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// C (16x8, fp32) += A (16x16, bf16, rows) * B (16x8, bf16, columns).  The
+// path feeds at most 8 rows, so A's registers for rows 8-15 are zero and
+// C's c[2], c[3] stay zero.
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a2,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+// Shared-memory address of the 16-byte unit u (dims 8u..8u+7) of row `key` of
+// a tile stored as TMA writes it (chunks of 64 dims, 128-byte swizzle).
+template <int CHUNK_BYTES>
+__device__ __forceinline__ uint32_t tile_unit(uint32_t base, int key, int u) {
+  return base + static_cast<uint32_t>((u >> 3) * CHUNK_BYTES + key * 128 +
+                                      (((u & 7) ^ (key & 7)) << 4));
+}
+
+// ---- 2..8 query rows: one warp-level MMA tile per 8 keys.  The rows are the
+// M dimension of mma.m16n8k16 (rows nq..15 are zero), so Q sits in A
+// fragments for the whole slice, K and V are read once per warp with
+// ldmatrix, and P stays in registers between S = Q K^T and O += P V (the
+// accumulator of two 8-key tiles is the A fragment of the next MMA).  Lane L
+// works on query row L / 4 (g) and, in each 8-key tile, keys 2(L % 4) and
+// 2(L % 4)+1 (c).
+template <int D>
+struct DecMmaRows {
+  float m = -INFINITY;  // running max of row g (base 2)
+  float l = 0.f;        // sum of the probabilities (fp32; for LSE)
+  float lo = 0.f;       // sum of the probabilities as rounded for P.V (for O)
+  float o[D / 8][4];    // O fragments: [dims 8n..8n+7][row g: c, c+1 | row g+8: 0, 0]
+};
+
+template <int D>
+__device__ __forceinline__ void decode_rows_mma(DecMmaRows<D>& st, const DecodeParams& p,
+                                                uint32_t sbase, uint64_t* full, uint64_t* empty,
+                                                const WaitCtl& ctl, int plane, int k_begin,
+                                                int k_end, int ntiles, int grp, int wq, int lane,
+                                                bool& ok) {
+  using C = DecCfg<D>;
+  constexpr int NS = C::NSTAGE;
+  const int g = lane >> 2, c = lane & 3;
+  // Q rows 0..7 as A fragments: [k block of 16 dims][dims 2c, 2c+1 | 2c+8, 2c+9]
+  uint32_t qa[D / 16][2];
+  const uint32_t* qg = reinterpret_cast<const uint32_t*>(
+      static_cast<const uint16_t*>(p.q) +
+      (static_cast<size_t>(plane) * p.nq + (g < p.nq ? g : 0)) * D);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    qa[kk][0] = (g < p.nq) ? qg[8 * kk + c] : 0u;
+    qa[kk][1] = (g < p.nq) ? qg[8 * kk + 4 + c] : 0u;
+  }
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) st.o[n][e] = 0.f;
+  for (int t = grp; t < ntiles; t += 2) {
+    const int s = t % NS;
+    // the ring protocol of the scalar path (see there)
+    if (t >= NS && !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((t / NS) - 1) & 1, ctl))) {
+      ok = false;
+      break;
+    }
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (t / NS) & 1, ctl))) {
+      ok = false;
+      break;
+    }
+    const uint32_t kt = sbase + C::K_OFF + s * C::TILE_BYTES;
+    const uint32_t vt = sbase + C::V_OFF + s * C::TILE_BYTES;
+    const int kw = 32 * wq;  // this warp's first key within the tile
+    // S = Q K^T for the warp's 32 keys: four 8-key tiles
+    float sa[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sa[nt][e] = 0.f;
+#pragma unroll
+      for (int kp = 0; kp < D / 32; ++kp) {
+        // dims 32kp + 8(L/8) .. +7 of key kw + 8nt + L%8: B fragments of two k blocks
+        uint32_t b[4];
+        ldsm_x4(tile_unit<C::CHUNK_BYTES>(kt, kw + 8 * nt + (lane & 7), 4 * kp + (lane >> 3)), b);
+        mma_bf16_16816(sa[nt], qa[2 * kp][0], qa[2 * kp][1], b[0], b[1]);
+        mma_bf16_16816(sa[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], b[2], b[3]);
+      }
+    }
+    // online softmax of row g over the 32 keys (4 lanes share a row)
+    const int key0 = k_begin + t * C::TK + kw + 2 * c;
+    float x[8];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        x[2 * nt + h] = (key0 + 8 * nt + h < k_end) ? sa[nt][h] * p.scale_log2 : -INFINITY;
+    float mx = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
+                     fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(st.m, mx);
+    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+    const float alpha = ex2_approx(st.m - m_use);
+    uint32_t pa[4];
+    float sum = 0.f, sum_r = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const float p0 = ex2_approx(x[2 * nt] - m_use);
+      const float p1 = ex2_approx(x[2 * nt + 1] - m_use);
+      pa[nt] = pack_bf16x2(p0, p1);
+      sum += p0 + p1;
+      sum_r += bf16lo(pa[nt]) + bf16hi(pa[nt]);
+    }
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    sum_r += __shfl_xor_sync(0xffffffffu, sum_r, 1);
+    sum_r += __shfl_xor_sync(0xffffffffu, sum_r, 2);
+    st.l = st.l * alpha + sum;
+    st.lo = st.lo * alpha + sum_r;
+    st.m = m_new;
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      st.o[n][0] *= alpha;
+      st.o[n][1] *= alpha;
+    }
+    // O += P V: two k steps of 16 keys; V's rows are keys, so B comes transposed
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+#pragma unroll
+      for (int np = 0; np < D / 16; ++np) {
+        // matrix L/8: keys +8((L/8)&1), dims 16np + 8((L/8)>>1)
+        const int i = lane >> 3;
+        uint32_t b[4];
+        ldsm_x4_trans(tile_unit<C::CHUNK_BYTES>(vt, kw + 16 * ks + 8 * (i & 1) + (lane & 7),
+                                                2 * np + (i >> 1)),
+                      b);
+        mma_bf16_16816(st.o[2 * np], pa[2 * ks], pa[2 * ks + 1], b[0], b[1]);
+        mma_bf16_16816(st.o[2 * np + 1], pa[2 * ks], pa[2 * ks + 1], b[2], b[3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+}
+
+// The warp's partial (m, l, l_o, O) of its rows into the merge arrays.
+template <int D>
+__device__ __forceinline__ void decode_rows_mma_store(const DecMmaRows<D>& st, float* ms,
+                                                      float* ls, float* los, float* os, int warp,
+                                                      int lane, int nq) {
+  const int g = lane >> 2, c = lane & 3;
+  if (g >= nq) return;
+  const int row = warp * kDecodeMaxQ + g;
+  if (c == 0) {
+    ms[row] = st.m;
+    ls[row] = st.l;
+    los[row] = st.lo;
+  }
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n)
+    *reinterpret_cast<float2*>(os + row * D + 8 * n + 2 * c) = make_float2(st.o[n][0], st.o[n][1]);
+}
+
+// NQ = 1: one query row per plane on CUDA cores (lane = key for the scores);
+// NQ = 8: 2..8 rows through warp-level MMAs (decode_rows_mma).
 template <int D, int NQ>
 __global__ void __launch_bounds__(288)
     attn_decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -87,7 +268,8 @@ __global__ void __launch_bounds__(288)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF);
   float* qs = reinterpret_cast<float*>(smem + C::Q_OFF);
   float* ms = reinterpret_cast<float*>(smem + C::M_OFF);
-  float* ls = ms + C::WARPS * kDecodeMaxQ;
+  float* ls = ms + C::WARPS * kDecodeMaxQ;   // sums of the probabilities (for LSE)
+  float* los = ls + C::WARPS * kDecodeMaxQ;  // sums of the weights P.V used (for O)
   float* os = reinterpret_cast<float*>(smem + C::O_OFF);
 
   const int plane = blockIdx.x / p.nsplit;
@@ -107,8 +289,10 @@ __global__ void __launch_bounds__(288)
     mbar_fence_init();
   }
   const uint16_t* qg = static_cast<const uint16_t*>(p.q) + static_cast<size_t>(plane) * nq * D;
-  for (int i = threadIdx.x; i < nq * D; i += blockDim.x)
-    qs[i] = __uint_as_float(static_cast<uint32_t>(qg[i]) << 16);
+  if constexpr (NQ == 1) {  // the scalar path reads Q from shared memory as fp32
+    for (int i = threadIdx.x; i < nq * D; i += blockDim.x)
+      qs[i] = __uint_as_float(static_cast<uint32_t>(qg[i]) << 16);
+  }
   __syncthreads();
   const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
   const uint32_t sbase = smem_u32(smem);
@@ -132,6 +316,10 @@ __global__ void __launch_bounds__(288)
     for (int d = max(0, t - NS); d < t; ++d) mbar_wait_drain(&full[d % NS], (d / NS) & 1, ctl);
   } else {
     // ------------------------------------------------------------ compute warps
+    const int grp = warp / 4;               // tiles t with t % 2 == grp
+    const int wq = warp % 4;                // key quarter within a tile
+    bool ok = true;
+    if constexpr (NQ == 1) {
     float m[NQ], l[NQ], o[NQ][C::CPL];
 #pragma unroll
     for (int qi = 0; qi < NQ; ++qi) {
@@ -140,10 +328,7 @@ __global__ void __launch_bounds__(288)
 #pragma unroll
       for (int e = 0; e < C::CPL; ++e) o[qi][e] = 0.f;
     }
-    const int grp = warp / 4;               // tiles t with t % 2 == grp
-    const int wq = warp % 4;                // key quarter within a tile
     const int r = 32 * wq + lane;           // this lane's key row within a tile
-    bool ok = true;
     for (int t = grp; t < ntiles; t += 2) {
       const int s = t % NS;
       // The two groups read the ring in interleaved order, so the previous use
@@ -266,12 +451,22 @@ __global__ void __launch_bounds__(288)
           if (lane == 0) {
             ms[warp * kDecodeMaxQ + qi] = m[qi];
             ls[warp * kDecodeMaxQ + qi] = l[qi];
+            los[warp * kDecodeMaxQ + qi] = l[qi];  // P.V used the fp32 P itself
           }
 #pragma unroll
           for (int e = 0; e < C::CPL; ++e)
             os[(warp * kDecodeMaxQ + qi) * D + C::CPL * lane + e] = o[qi][e];
         }
       }
+    }
+    } else {
+      DecMmaRows<D> st;
+      decode_rows_mma<D>(st, p, sbase, full, empty, ctl, plane, k_begin, k_end, ntiles, grp, wq,
+                         lane, ok);
+      // merge the eight warps through shared memory, as above
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * C::WARPS) : "memory");
+      ok = !*abort_flag;
+      if (ok) decode_rows_mma_store<D>(st, ms, ls, los, os, warp, lane, nq);
     }
     asm volatile("bar.sync 1, %0;" ::"n"(32 * C::WARPS) : "memory");
     if (ok && !*abort_flag) {
@@ -281,14 +476,15 @@ __global__ void __launch_bounds__(288)
 #pragma unroll
         for (int w = 0; w < C::WARPS; ++w) mt = fmaxf(mt, ms[w * kDecodeMaxQ + qi]);
         const float mu = (mt == -INFINITY) ? 0.f : mt;
-        float lt = 0.f, ot = 0.f;
+        float lt = 0.f, lot = 0.f, ot = 0.f;
 #pragma unroll
         for (int w = 0; w < C::WARPS; ++w) {
           const float f = ex2_approx(ms[w * kDecodeMaxQ + qi] - mu);
           lt += f * ls[w * kDecodeMaxQ + qi];
+          lot += f * los[w * kDecodeMaxQ + qi];
           ot += f * os[(w * kDecodeMaxQ + qi) * D + d];
         }
-        const float out = ot / lt;
+        const float out = (lot > 0.f) ? ot / lot : 0.f;
         const float lse = (mu + log2f(lt)) * 0.69314718055994530942f;
         if (p.nsplit == 1) {
           const size_t g = static_cast<size_t>(plane) * nq + qi;
