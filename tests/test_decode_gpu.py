@@ -77,3 +77,38 @@ def test_decode_single_key_is_that_value():
     q, k, v = _draw(2, 2, 3, 1, 128, seed=4)
     o, lse = _run(q, k, v, 0.125)
     np.testing.assert_array_equal(o, np.broadcast_to(W.as_f64(v), o.shape))
+
+
+# 2..8 query rows take the warp-level MMA path: every row count, both head
+# dims, ragged and long caches, and the score regimes at both ends.
+
+@pytest.mark.parametrize("Nq", [2, 4, 5, 6, 7])
+@pytest.mark.parametrize("Nk", [129, 5000])
+@pytest.mark.parametrize("D", [64, 128])
+def test_decode_every_row_count(Nq, Nk, D):
+    q, k, v = _draw(2, 2, Nq, Nk, D, seed=100 + Nq + Nk + D)
+    scale = float(np.float32(1 / np.sqrt(D)))
+    o, lse = _run(q, k, v, scale)
+    ro, rl = oracle.attention(W.as_f64(q), W.as_f64(k), W.as_f64(v), scale, False)
+    assert max_err(o, ro) <= BF16_TOL_O and max_err(lse, rl) <= BF16_TOL_LSE
+
+
+@pytest.mark.parametrize("scale", [1e-3, 2.0])
+@pytest.mark.parametrize("Nq", [1, 4, 8])
+def test_decode_extreme_scales(scale, Nq):
+    # near-uniform rows, and one-hot rows whose weight of 1 is exact in bf16
+    q, k, v = _draw(2, 3, Nq, 3000, 128, seed=200 + Nq)
+    o, lse = _run(q, k, v, scale)
+    ro, rl = oracle.attention(W.as_f64(q), W.as_f64(k), W.as_f64(v), scale, False)
+    assert max_err(o, ro) <= BF16_TOL_O and max_err(lse, rl) <= BF16_TOL_LSE
+
+
+def test_decode_eight_rows_long_cache_sampled_heads():
+    q, k, v = _draw(8, 32, 8, 32768, 128, seed=9)
+    scale = float(np.float32(1 / np.sqrt(128)))
+    o, lse = _run(q, k, v, scale)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    for b, h in ((0, 0), (5, 9), (7, 31)):
+        ro, rl = oracle.attention_plane(W.as_f64(q[b, h]), W.as_f64(k[b, h]), W.as_f64(v[b, h]),
+                                        scale, False)
+        assert max_err(o[b, h], ro) <= BF16_TOL_O and max_err(lse[b, h], rl) <= BF16_TOL_LSE
