@@ -49,9 +49,9 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
-template <int D, int NQ>
+template <int D>
 bool set_decode_smem() {
-  return cudaFuncSetAttribute(attn_decode_bf16_kernel<D, NQ>,
+  return cudaFuncSetAttribute(attn_decode_bf16_kernel<D>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               DecCfg<D>::SMEM_ALLOC) != cudaSuccess;
 }
@@ -59,11 +59,7 @@ bool set_decode_smem() {
 template <int D>
 void launch_decode_kernel(unsigned grid, cudaStream_t s, const CUtensorMap& mk,
                           const CUtensorMap& mv, const DecodeParams& p) {
-  constexpr int T = DecCfg<D>::THREADS, SM = DecCfg<D>::SMEM_ALLOC;
-  if (p.nq <= 1)
-    attn_decode_bf16_kernel<D, 1><<<grid, T, SM, s>>>(mk, mv, p);
-  else
-    attn_decode_bf16_kernel<D, 8><<<grid, T, SM, s>>>(mk, mv, p);
+  attn_decode_bf16_kernel<D><<<grid, DecCfg<D>::THREADS, DecCfg<D>::SMEM_ALLOC, s>>>(mk, mv, p);
 }
 
 // Checks the current device once and fetches what the launches need.
@@ -127,8 +123,7 @@ int prepare_device(DeviceState** out) {
       cudaGetLastError();
       return ATTN_ERR_LAUNCH;
     }
-    if (set_decode_smem<64, 1>() || set_decode_smem<64, 8>() || set_decode_smem<128, 1>() ||
-        set_decode_smem<128, 8>()) {
+    if (set_decode_smem<64>() || set_decode_smem<128>()) {
       cudaGetLastError();
       return ATTN_ERR_LAUNCH;
     }

@@ -17,14 +17,12 @@
 // one TMA producer warp.  Keys arrive in the forward kernel's swizzled tile
 // layout; warp w of a group works on keys 32w..32w+31 of its tile, keeps its
 // own running max / sums / output for the query rows, and the eight warps are
-// merged at the end.  One query row (NQ = 1) runs on CUDA cores: lane = key
-// for the scores (the row reads of the 32 lanes hit distinct banks thanks to
-// the swizzle), and for P.V lane l accumulates output columns
-// [D/32 * l, D/32 * (l+1)).  Two to eight rows (NQ = 8) run as warp-level
-// MMAs with the rows as the M dimension (decode_rows_mma): on CUDA cores the
-// work per key grows with the rows and, from two rows on, outweighs the HBM
-// read of the key.  There P is rounded to bf16 for P.V, and O is divided by
-// the sum of the rounded weights (LSE keeps the fp32 sum).
+// merged at the end.  The 1..8 query rows are the M dimension of warp-level
+// MMAs (decode_rows_mma), so each key is read once per warp with ldmatrix and
+// scored against every row at once; on CUDA cores (lane = key) the work per
+// key grew with the rows and already bounded a single row below the HBM
+// rate.  P is rounded to bf16 for P.V, and O is divided by the sum of the
+// rounded weights (LSE keeps the fp32 sum).
 #pragma once
 
 #include "ptx.cuh"
@@ -58,8 +56,7 @@ struct DecCfg {
   static constexpr int TILE_BYTES = TK * D * 2;
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = NSTAGE * TILE_BYTES;
-  static constexpr int Q_OFF = 2 * NSTAGE * TILE_BYTES;          // float [MAXQ][D]
-  static constexpr int BAR_OFF = Q_OFF + kDecodeMaxQ * D * 4;
+  static constexpr int BAR_OFF = 2 * NSTAGE * TILE_BYTES;
   static constexpr int NBAR = 2 * NSTAGE;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM_ALLOC = MISC_OFF + 16 + 1024;
@@ -69,15 +66,14 @@ struct DecCfg {
   static constexpr int O_OFF = 3 * 8 * kDecodeMaxQ * 4;
   static constexpr int WARPS = 8;                                 // compute warps
   static constexpr int THREADS = 32 * WARPS + 32;
-  static constexpr int CPL = D / 32;                             // output columns per lane
-  static_assert(O_OFF + WARPS * kDecodeMaxQ * D * 4 <= Q_OFF, "merge area fits the stages");
+  static_assert(O_OFF + WARPS * kDecodeMaxQ * D * 4 <= BAR_OFF, "merge area fits the stages");
   static_assert(SMEM_ALLOC <= 232448, "shared memory");
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
-// ---- warp-level tensor-core helpers for the 2..8-row path
+// ---- warp-level tensor-core helpers
 // Four 8x8 16-bit matrices from shared memory; lane L gives the address of row
 // L % 8 of matrix L / 8 and receives (row L / 4, columns 2(L % 4), 2(L % 4)+1)
 // of each matrix (with .trans: rows 2(L % 4), 2(L % 4)+1 of column L / 4).
@@ -92,7 +88,7 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
                : "r"(addr));
 }
 // C (16x8, fp32) += A (16x16, bf16, rows) * B (16x8, bf16, columns).  The
-// path feeds at most 8 rows, so A's registers for rows 8-15 are zero and
+// kernel feeds at most 8 rows, so A's registers for rows 8-15 are zero and
 // C's c[2], c[3] stay zero.
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a2,
                                                uint32_t b0, uint32_t b1) {
@@ -110,7 +106,7 @@ __device__ __forceinline__ uint32_t tile_unit(uint32_t base, int key, int u) {
                                       (((u & 7) ^ (key & 7)) << 4));
 }
 
-// ---- 2..8 query rows: one warp-level MMA tile per 8 keys.  The rows are the
+// ---- 1..8 query rows: one warp-level MMA tile per 8 keys.  The rows are the
 // M dimension of mma.m16n8k16 (rows nq..15 are zero), so Q sits in A
 // fragments for the whole slice, K and V are read once per warp with
 // ldmatrix, and P stays in registers between S = Q K^T and O += P V (the
@@ -150,7 +146,11 @@ __device__ __forceinline__ void decode_rows_mma(DecMmaRows<D>& st, const DecodeP
     for (int e = 0; e < 4; ++e) st.o[n][e] = 0.f;
   for (int t = grp; t < ntiles; t += 2) {
     const int s = t % NS;
-    // the ring protocol of the scalar path (see there)
+    // The two groups read the ring in interleaved order, so the previous use
+    // of this stage (tile t - NS) belongs to the other group and may not have
+    // landed yet; a parity wait on full[s] would then match the phase of
+    // tile t - 2*NS.  Waiting first until tile t - NS has been read (its
+    // empty phase) puts full[s] in tile t's phase, one phase apart at most.
     if (t >= NS && !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((t / NS) - 1) & 1, ctl))) {
       ok = false;
       break;
@@ -252,9 +252,8 @@ __device__ __forceinline__ void decode_rows_mma_store(const DecMmaRows<D>& st, f
     *reinterpret_cast<float2*>(os + row * D + 8 * n + 2 * c) = make_float2(st.o[n][0], st.o[n][1]);
 }
 
-// NQ = 1: one query row per plane on CUDA cores (lane = key for the scores);
-// NQ = 8: 2..8 rows through warp-level MMAs (decode_rows_mma).
-template <int D, int NQ>
+// The decode kernel: key slices of a plane per CTA, 1..8 query rows.
+template <int D>
 __global__ void __launch_bounds__(288)
     attn_decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
@@ -266,7 +265,6 @@ __global__ void __launch_bounds__(288)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* empty = full + NS;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF);
-  float* qs = reinterpret_cast<float*>(smem + C::Q_OFF);
   float* ms = reinterpret_cast<float*>(smem + C::M_OFF);
   float* ls = ms + C::WARPS * kDecodeMaxQ;   // sums of the probabilities (for LSE)
   float* los = ls + C::WARPS * kDecodeMaxQ;  // sums of the weights P.V used (for O)
@@ -287,11 +285,6 @@ __global__ void __launch_bounds__(288)
     }
     *abort_flag = 0;
     mbar_fence_init();
-  }
-  const uint16_t* qg = static_cast<const uint16_t*>(p.q) + static_cast<size_t>(plane) * nq * D;
-  if constexpr (NQ == 1) {  // the scalar path reads Q from shared memory as fp32
-    for (int i = threadIdx.x; i < nq * D; i += blockDim.x)
-      qs[i] = __uint_as_float(static_cast<uint32_t>(qg[i]) << 16);
   }
   __syncthreads();
   const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
@@ -316,158 +309,18 @@ __global__ void __launch_bounds__(288)
     for (int d = max(0, t - NS); d < t; ++d) mbar_wait_drain(&full[d % NS], (d / NS) & 1, ctl);
   } else {
     // ------------------------------------------------------------ compute warps
-    const int grp = warp / 4;               // tiles t with t % 2 == grp
-    const int wq = warp % 4;                // key quarter within a tile
+    const int grp = warp / 4;  // tiles t with t % 2 == grp
+    const int wq = warp % 4;   // key quarter within a tile
     bool ok = true;
-    if constexpr (NQ == 1) {
-    float m[NQ], l[NQ], o[NQ][C::CPL];
-#pragma unroll
-    for (int qi = 0; qi < NQ; ++qi) {
-      m[qi] = -INFINITY;
-      l[qi] = 0.f;
-#pragma unroll
-      for (int e = 0; e < C::CPL; ++e) o[qi][e] = 0.f;
-    }
-    const int r = 32 * wq + lane;           // this lane's key row within a tile
-    for (int t = grp; t < ntiles; t += 2) {
-      const int s = t % NS;
-      // The two groups read the ring in interleaved order, so the previous use
-      // of this stage (tile t - NS) belongs to the other group and may not have
-      // landed yet; a parity wait on full[s] would then match the phase of
-      // tile t - 2*NS.  Waiting first until tile t - NS has been read (its
-      // empty phase) puts full[s] in tile t's phase, one phase apart at most.
-      if (t >= NS && !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((t / NS) - 1) & 1, ctl))) {
-        ok = false;
-        break;
-      }
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (t / NS) & 1, ctl))) {
-        ok = false;
-        break;
-      }
-      const uint8_t* kt = smem + C::K_OFF + s * C::TILE_BYTES;
-      const uint8_t* vt = smem + C::V_OFF + s * C::TILE_BYTES;
-      // scores of this lane's key against every query row
-      float sc4[NQ][4];
-#pragma unroll
-      for (int qi = 0; qi < NQ; ++qi)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sc4[qi][e] = 0.f;
-#pragma unroll
-      for (int u = 0; u < D / 8; ++u) {
-        const int phys = (u % 8) ^ (r & 7);
-        const uint4 kv = *reinterpret_cast<const uint4*>(kt + (u / 8) * C::CHUNK_BYTES + r * 128 +
-                                                         phys * 16);
-        const float kf[8] = {bf16lo(kv.x), bf16hi(kv.x), bf16lo(kv.y), bf16hi(kv.y),
-                             bf16lo(kv.z), bf16hi(kv.z), bf16lo(kv.w), bf16hi(kv.w)};
-#pragma unroll
-        for (int qi = 0; qi < NQ; ++qi) {
-          if (qi < nq) {
-            const float4 q0 = *reinterpret_cast<const float4*>(qs + qi * D + u * 8);
-            const float4 q1 = *reinterpret_cast<const float4*>(qs + qi * D + u * 8 + 4);
-            sc4[qi][0] = fmaf(q0.x, kf[0], sc4[qi][0]);
-            sc4[qi][1] = fmaf(q0.y, kf[1], sc4[qi][1]);
-            sc4[qi][2] = fmaf(q0.z, kf[2], sc4[qi][2]);
-            sc4[qi][3] = fmaf(q0.w, kf[3], sc4[qi][3]);
-            sc4[qi][0] = fmaf(q1.x, kf[4], sc4[qi][0]);
-            sc4[qi][1] = fmaf(q1.y, kf[5], sc4[qi][1]);
-            sc4[qi][2] = fmaf(q1.z, kf[6], sc4[qi][2]);
-            sc4[qi][3] = fmaf(q1.w, kf[7], sc4[qi][3]);
-          }
-        }
-      }
-      float sc[NQ];
-#pragma unroll
-      for (int qi = 0; qi < NQ; ++qi)
-        sc[qi] = (sc4[qi][0] + sc4[qi][1]) + (sc4[qi][2] + sc4[qi][3]);
-      const bool valid = k_begin + t * C::TK + r < k_end;
-      // online softmax per query row, over this warp's 32 keys, in base 2
-      float pj[NQ];
-#pragma unroll
-      for (int qi = 0; qi < NQ; ++qi) {
-        if (qi < nq) {
-          const float x = valid ? sc[qi] * p.scale_log2 : -INFINITY;
-          float mx = x;
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1)
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-          const float m_new = fmaxf(m[qi], mx);
-          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-          const float alpha = ex2_approx(m[qi] - m_use);
-          const float pv = ex2_approx(x - m_use);
-          float sum = pv;
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-          l[qi] = l[qi] * alpha + sum;
-#pragma unroll
-          for (int e = 0; e < C::CPL; ++e) o[qi][e] *= alpha;
-          m[qi] = m_new;
-          pj[qi] = pv;
-        }
-      }
-      // P.V: lane l owns columns [CPL*l, CPL*(l+1))
-#pragma unroll 4
-      for (int j = 0; j < 32; ++j) {
-        const int rv = 32 * wq + j;
-        float vf[C::CPL];
-        if constexpr (D == 128) {
-          const int c = lane / 16;
-          const int byte = 8 * (lane % 16);
-          const int phys = (byte / 16) ^ (rv & 7);
-          const uint2 vv = *reinterpret_cast<const uint2*>(vt + c * C::CHUNK_BYTES + rv * 128 +
-                                                           phys * 16 + (byte % 16));
-          vf[0] = bf16lo(vv.x);
-          vf[1] = bf16hi(vv.x);
-          vf[C::CPL > 2 ? 2 : 0] = bf16lo(vv.y);
-          vf[C::CPL > 3 ? 3 : 0] = bf16hi(vv.y);
-        } else {
-          const int byte = 4 * lane;
-          const int phys = (byte / 16) ^ (rv & 7);
-          const uint32_t vv =
-              *reinterpret_cast<const uint32_t*>(vt + rv * 128 + phys * 16 + (byte % 16));
-          vf[0] = bf16lo(vv);
-          vf[C::CPL > 1 ? 1 : 0] = bf16hi(vv);
-        }
-#pragma unroll
-        for (int qi = 0; qi < NQ; ++qi) {
-          if (qi < nq) {
-            const float pb = __shfl_sync(0xffffffffu, pj[qi], j);
-#pragma unroll
-            for (int e = 0; e < C::CPL; ++e) o[qi][e] = fmaf(pb, vf[e], o[qi][e]);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-    }
+    DecMmaRows<D> st;
+    decode_rows_mma<D>(st, p, sbase, full, empty, ctl, plane, k_begin, k_end, ntiles, grp, wq,
+                       lane, ok);
     // merge the eight warps through shared memory (the drained K/V stages):
     // every compute warp must be past its last tile before the area is reused
     asm volatile("bar.sync 1, %0;" ::"n"(32 * C::WARPS) : "memory");
     // after an abort, copies may still be landing in the stages: skip the merge
     ok = !*abort_flag;
-    if (ok) {
-#pragma unroll
-      for (int qi = 0; qi < NQ; ++qi) {
-        if (qi < nq) {
-          if (lane == 0) {
-            ms[warp * kDecodeMaxQ + qi] = m[qi];
-            ls[warp * kDecodeMaxQ + qi] = l[qi];
-            los[warp * kDecodeMaxQ + qi] = l[qi];  // P.V used the fp32 P itself
-          }
-#pragma unroll
-          for (int e = 0; e < C::CPL; ++e)
-            os[(warp * kDecodeMaxQ + qi) * D + C::CPL * lane + e] = o[qi][e];
-        }
-      }
-    }
-    } else {
-      DecMmaRows<D> st;
-      decode_rows_mma<D>(st, p, sbase, full, empty, ctl, plane, k_begin, k_end, ntiles, grp, wq,
-                         lane, ok);
-      // merge the eight warps through shared memory, as above
-      asm volatile("bar.sync 1, %0;" ::"n"(32 * C::WARPS) : "memory");
-      ok = !*abort_flag;
-      if (ok) decode_rows_mma_store<D>(st, ms, ls, los, os, warp, lane, nq);
-    }
+    if (ok) decode_rows_mma_store<D>(st, ms, ls, los, os, warp, lane, nq);
     asm volatile("bar.sync 1, %0;" ::"n"(32 * C::WARPS) : "memory");
     if (ok && !*abort_flag) {
       for (int i = threadIdx.x; i < nq * D; i += 32 * C::WARPS) {
