@@ -166,7 +166,8 @@ def system_info(dev) -> dict:
     import torch
     prop = torch.cuda.get_device_properties(dev)
     info = {"sms": prop.multi_processor_count, "cc": f"{prop.major}.{prop.minor}",
-            "torch": torch.__version__, "cuda_runtime": torch.version.cuda}
+            "torch": torch.__version__, "cuda_runtime": torch.version.cuda,
+            "host_cores": host_cores(), "cgroup_cpu_limit": cgroup_cpu_limit()}
     try:
         out = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader",
                               "-i", str(torch.cuda.current_device())],
@@ -210,11 +211,32 @@ def barrier(ws: int):
 # CPU oracle timing (the cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def host_cores() -> int:
+def cgroup_cpu_limit():
+    """CPUs' worth of time the cgroup quota allows this process (None: no quota)."""
     try:
-        return len(os.sched_getaffinity(0))
+        quota, period = open("/sys/fs/cgroup/cpu.max").read().split()[:2]
+        if quota != "max" and int(period) > 0:
+            return max(1, -(-int(quota) // int(period)))
+    except (OSError, ValueError):
+        pass
+    try:
+        quota = int(open("/sys/fs/cgroup/cpu/cpu.cfs_quota_us").read())
+        period = int(open("/sys/fs/cgroup/cpu/cpu.cfs_period_us").read())
+        if quota > 0 and period > 0:
+            return max(1, -(-quota // period))
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+def host_cores() -> int:
+    """Cores this process may run on: the affinity mask, capped by a cgroup CPU quota."""
+    try:
+        n = len(os.sched_getaffinity(0))
     except AttributeError:
-        return os.cpu_count() or 1
+        n = os.cpu_count() or 1
+    q = cgroup_cpu_limit()
+    return min(n, q) if q else n
 
 
 def _blas_single_thread():
@@ -227,47 +249,136 @@ def _blas_single_thread():
         return contextlib.nullcontext()
 
 
-def oracle_rows_sample(w, x, plane_index: int, rows: np.ndarray, threads: int):
-    """Run the oracle on the given rows of one plane; returns (flops, seconds)."""
+def _rows_flops(w, rows: np.ndarray) -> float:
+    """Attention FLOPs of the given query rows (4 D per allowed key)."""
+    nk = w.n_keys
+    keys = np.clip(rows + 1 + (nk - w.N), 0, nk) if w.causal else np.full(len(rows), nk)
+    return float(4.0 * w.D * keys.sum())
+
+
+def oracle_rows_sample(w, x, plane_index: int, rows: np.ndarray, threads: int = 1):
+    """Run the oracle on the given rows of one plane in this process; returns (flops, seconds)."""
     import oracle
-    from concurrent.futures import ThreadPoolExecutor
     b, h = divmod(plane_index, w.H)
     q = W.as_f64(x["q"][b, h])
     k = W.as_f64(x["k"][b, h])
     v = W.as_f64(x["v"][b, h])
-    chunks = [c for c in np.array_split(rows, max(1, threads)) if len(c)]
     with _blas_single_thread():
         t0 = time.perf_counter()
-        with ThreadPoolExecutor(max_workers=threads) as ex:
-            list(ex.map(lambda r: oracle.attention_rows(q, k, v, w.scale, w.causal, r), chunks))
+        oracle.attention_rows(q, k, v, w.scale, w.causal, rows)
         dt = time.perf_counter() - t0
-    nk = w.n_keys
-    keys = np.clip(rows + 1 + (nk - w.N), 0, nk) if w.causal else np.full(len(rows), nk)
-    flops = float(4.0 * w.D * keys.sum())
-    return flops, dt
+    return _rows_flops(w, rows), dt
+
+
+_ORACLE_PLANE = None
+
+
+def _oracle_worker_init(q, k, v, scale, causal):
+    global _ORACLE_PLANE
+    _ORACLE_PLANE = (q, k, v, scale, causal)
+    try:
+        from threadpoolctl import threadpool_limits
+        threadpool_limits(limits=1)
+    except ImportError:
+        pass
+
+
+def _oracle_worker_rows(rows):
+    import oracle
+    q, k, v, scale, causal = _ORACLE_PLANE
+    oracle.attention_rows(q, k, v, scale, causal, rows)
+    return len(rows)
+
+
+class OraclePool:
+    """The oracle on rows of one plane, row-parallel over spawned processes (one
+    BLAS thread each).  Processes, not threads: the per-row NumPy work is too
+    small to run in parallel under the interpreter lock.  Spawned, not forked:
+    a process forked after CUDA has been initialised can hang."""
+
+    def __init__(self, w, x, plane_index: int, procs: int):
+        import multiprocessing as mp
+        from concurrent.futures import ProcessPoolExecutor
+        b, h = divmod(plane_index, w.H)
+        init = (W.as_f64(x["q"][b, h]), W.as_f64(x["k"][b, h]), W.as_f64(x["v"][b, h]),
+                w.scale, w.causal)
+        self.w, self.x, self.plane, self.procs = w, x, plane_index, procs
+        self.ex = ProcessPoolExecutor(max_workers=procs, mp_context=mp.get_context("spawn"),
+                                      initializer=_oracle_worker_init, initargs=init)
+        # start every worker before anything is timed; a pool that does not come
+        # up (a worker that cannot start) falls back to this process alone
+        try:
+            list(self.ex.map(_oracle_worker_rows, [np.arange(1)] * (2 * procs), timeout=180))
+        except Exception:  # noqa: BLE001 - any failure: measure in-process instead
+            self.ex.shutdown(wait=False, cancel_futures=True)
+            self.ex, self.procs = None, 1
+
+    def run(self, rows: np.ndarray):
+        """(flops, seconds) of the oracle on `rows`, dealt round-robin so that
+        long and short causal rows spread evenly over the processes."""
+        if self.ex is None:
+            return oracle_rows_sample(self.w, self.x, self.plane, rows)
+        chunks = [rows[i::self.procs] for i in range(self.procs) if len(rows[i::self.procs])]
+        t0 = time.perf_counter()
+        list(self.ex.map(_oracle_worker_rows, chunks, timeout=600))
+        return _rows_flops(self.w, rows), time.perf_counter() - t0
+
+    def close(self):
+        if self.ex is not None:
+            self.ex.shutdown()
+
+
+def _sample_block(n: int, done: int, size: int) -> np.ndarray:
+    """The next block of the sample: the plane's rows from the last one backwards
+    (the full-length causal rows first), starting over once all have been used."""
+    r1 = n - (done % n)
+    return np.arange(max(0, r1 - size), r1)
 
 
 def cpu_baseline(w, x, budget_s: float = 12.0):
-    """Oracle throughput on a bounded sample: the last rows of plane 0 (full-length causal rows)."""
-    threads = host_cores()
-    n_rows = 256
-    flops_total, t_total, rows_done = 0.0, 0.0, 0
-    while t_total < budget_s and rows_done < w.N:
-        r1 = w.N - rows_done
-        rows = np.arange(max(0, r1 - n_rows), r1)
-        f, dt = oracle_rows_sample(w, x, 0, rows, threads)
-        flops_total += f
-        t_total += dt
-        rows_done += len(rows)
-        n_rows = min(4096, n_rows * 2)
-    # the same oracle on one core, on the last 256 rows
+    """Oracle throughput on a bounded sample: the last rows of plane 0 (full-length causal rows),
+    dealt over a process per core; if that turns out slower than one process (a host whose
+    cores are shared or throttled), one process on the same budget."""
+    procs = host_cores()
+    # the same oracle in one process, on the last 256 rows
     one = np.arange(max(0, w.N - 256), w.N)
-    f1, dt1 = oracle_rows_sample(w, x, 0, one, 1)
-    return {"value": flops_total / t_total / 1e12, "unit": "TFLOP/s", "cores": threads,
-            "kind": "oracle", "value_1core": f1 / dt1 / 1e12,
-            "sample": f"fp64 oracle on the last {rows_done} query rows of plane (b=0,h=0) "
-                      f"of {w.name} ({t_total:.1f} s of CPU work, {threads} threads); "
-                      f"value_1core: the last {len(one)} rows on one thread ({dt1:.2f} s)"}
+    f1, dt1 = oracle_rows_sample(w, x, 0, one)
+    v1 = f1 / dt1 / 1e12
+    pool = OraclePool(w, x, 0, procs)
+    try:
+        n_rows = 256
+        flops_total, t_total, rows_done = 0.0, 0.0, 0
+        while t_total < budget_s:
+            rows = _sample_block(w.N, rows_done, n_rows)
+            f, dt = pool.run(rows)
+            flops_total += f
+            t_total += dt
+            rows_done += len(rows)
+            n_rows = min(16384, n_rows * 2)
+    finally:
+        pool.close()
+    procs = pool.procs
+    value = flops_total / t_total / 1e12
+    how = f"rows dealt over {procs} processes"
+    if procs > 1 and value < v1:
+        # more processes than the host really runs at once: one process instead
+        flops_total, t_total, rows_done, n_rows = 0.0, 0.0, 0, 256
+        while t_total < budget_s:
+            rows = _sample_block(w.N, rows_done, n_rows)
+            f, dt = oracle_rows_sample(w, x, 0, rows)
+            flops_total += f
+            t_total += dt
+            rows_done += len(rows)
+            n_rows = min(4096, n_rows * 2)
+        how = (f"one process ({procs} processes ran at {value:.2e} TFLOP/s, below one "
+               f"process: the host's cores are shared or throttled)")
+        value, procs = flops_total / t_total / 1e12, 1
+    return {"value": value, "unit": "TFLOP/s", "cores": procs,
+            "kind": "oracle", "value_1core": v1,
+            "sample": f"fp64 oracle on {rows_done} query rows of plane (b=0,h=0) of "
+                      f"{w.name} (from the last row backwards, starting over after row 0), "
+                      f"{how} ({t_total:.1f} s); "
+                      f"value_1core: the last {len(one)} rows in one process ({dt1:.2f} s)"}
 
 
 def run_reference(args, w):
@@ -277,13 +388,22 @@ def run_reference(args, w):
     x = W.generate(w)
     threads = host_cores()
     rows = np.arange(max(0, w.N - 512), w.N)   # one step: the last 512 rows of plane 0
-    for _ in range(args.warmup):
-        oracle_rows_sample(w, x, 0, rows, threads)
-    flops = secs = 0.0
-    for _ in range(args.steps):
-        f, dt = oracle_rows_sample(w, x, 0, rows, threads)
-        flops += f
-        secs += dt
+    pool = OraclePool(w, x, 0, threads)
+    try:
+        # a process per core, unless that is slower than one process on this host
+        _, t_one = oracle_rows_sample(w, x, 0, rows)
+        _, t_pool = pool.run(rows)
+        step = pool.run if t_pool < t_one else (lambda r: oracle_rows_sample(w, x, 0, r))
+        threads = pool.procs if t_pool < t_one else 1
+        for _ in range(args.warmup):
+            step(rows)
+        flops = secs = 0.0
+        for _ in range(args.steps):
+            f, dt = step(rows)
+            flops += f
+            secs += dt
+    finally:
+        pool.close()
     value = flops / secs / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
@@ -293,7 +413,8 @@ def run_reference(args, w):
         "config": workload_config(w),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": f"each step: fp64 oracle on query rows {rows[0]}..{rows[-1]} "
-                                   f"of plane (b=0,h=0) of {w.name}"},
+                                   f"of plane (b=0,h=0) of {w.name}, dealt over {threads} "
+                                   f"process(es)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
