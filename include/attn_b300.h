@@ -214,8 +214,10 @@ int attn_bwd_workspace_bytes(int B, int H, int Nq, int D, int packed, unsigned l
  * device workspace of attn_decode_workspace_bytes() bytes (16-byte aligned);
  * with workspace == NULL (or too small) every plane is processed by one
  * thread block instead, which is correct but slower for few planes.
- * Arithmetic: bf16 operands, fp32 scores, probabilities, sums and outputs;
- * O rounded to bf16 once.
+ * Arithmetic: bf16 operands, fp32 scores, sums and accumulators; the
+ * probabilities are rounded to bf16 for P.V (as in attn_fwd), O is divided by
+ * the sum of those rounded weights and LSE uses the fp32 sum; O is rounded to
+ * bf16 once.
  */
 int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int Nq, int Nk, int D, float scale, void* workspace,
