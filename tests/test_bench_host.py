@@ -159,3 +159,30 @@ def test_cross_generator_shapes():
 def test_cross_workload_config_keys(name):
     cfg = bench.workload_config(W.CROSS_WORKLOADS[name])
     assert cfg["workload"] == name and cfg["Nk"] == W.CROSS_WORKLOADS[name].n_keys
+
+
+def test_sample_blocks_walk_back_from_the_last_row_and_start_over():
+    blocks, done = [], 0
+    for size in (3, 3, 3, 3):
+        b = bench._sample_block(7, done, size)
+        blocks.append(b.tolist())
+        done += len(b)
+    # 7 rows: 4..6, 1..3, then the short block 0..0, then again from the end
+    assert blocks == [[4, 5, 6], [1, 2, 3], [0], [4, 5, 6]]
+
+
+def test_host_cores_respects_the_affinity_mask():
+    n = bench.host_cores()
+    assert 1 <= n <= len(os.sched_getaffinity(0))
+    q = bench.cgroup_cpu_limit()
+    assert q is None or q >= 1
+
+
+def test_cpu_baseline_on_a_small_workload():
+    # the process pool (spawned workers) and the one-process figure
+    w = W.WORKLOADS["f32_causal_b2_h4_n128_d64"]
+    x = W.generate(w)
+    r = bench.cpu_baseline(w, x, budget_s=0.5)
+    assert r["kind"] == "oracle" and r["value"] > 0 and r["value_1core"] > 0
+    assert 1 <= r["cores"] <= bench.host_cores()
+    assert "query rows of plane (b=0,h=0)" in r["sample"]
