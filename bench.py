@@ -1,20 +1,27 @@
 """Throughput of the exact attention forward on B300 (one JSON line on stdout).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-cpu-baseline]
+                    [--workload NAME] [--no-cpu-baseline] [--no-extra]
+                    [--op forward|backward|decode]
 
 A step is one attention forward over the whole workload (default: bf16,
 causal, B=2, H=32, N=8192, D=128).  ``value`` is device-timed TFLOP/s with
-inputs resident in HBM (CUDA events on the launching stream, K back-to-back
-launches; the inputs, 403 MB, exceed the 126 MB L2 so no flush is needed).
+inputs resident in HBM: the K steps are captured into one CUDA graph and its
+replay is timed with CUDA events on the launching stream (the inputs, 403 MB,
+exceed the 126 MB L2, so no flush is needed; workloads that fit in L2 are
+timed launch by launch with a 256 MB buffer written before each).  The step is
+one kernel, so ``roofline.achieved`` is that kernel's rate over the same time.
 ``e2e`` is the same metric through the C-ABI call on pinned host buffers
 (``attn_fwd_host``): every step copies Q, K, V host->device and O, LSE
 device->host inside the timed region, chunk by chunk, overlapped with the
-kernels.  Under torchrun each rank runs its own replica of the
+kernels.  ``workloads`` carries the other forward workloads, the backward on
+the headline shape and a KV-cache decode, each timed the same way with its
+own clocks and roofline.  Under torchrun each rank runs its own replica of the
 workload (weak scaling); the slowest rank's time is used.
 
-``--impl reference`` times the fp64 CPU oracle on the host cores instead,
-each step on a bounded sample of the same workload (rank 0 only).
+``cpu_baseline`` (and ``--impl reference``) times the fp64 CPU oracle on the
+host cores, whole planes at a time, one spawned process per core, on a
+bounded sample of the same workload (rank 0 only).
 """
 
 from __future__ import annotations
@@ -249,33 +256,61 @@ def _blas_single_thread():
         return contextlib.nullcontext()
 
 
-def _rows_flops(w, rows: np.ndarray) -> float:
-    """Attention FLOPs of the given query rows (4 D per allowed key)."""
-    nk = w.n_keys
-    keys = np.clip(rows + 1 + (nk - w.N), 0, nk) if w.causal else np.full(len(rows), nk)
-    return float(4.0 * w.D * keys.sum())
+# The oracle is timed in the form the parity tests run it: oracle.attention_plane
+# on whole planes (the full score matrix up to 4096 rows, 512-row slabs above),
+# one plane per task.  A unit of work is one plane, or its last UNIT_ROWS query
+# rows when it is longer (those rows see the most keys under the causal mask).
+UNIT_ROWS = 8192
 
 
-def oracle_rows_sample(w, x, plane_index: int, rows: np.ndarray, threads: int = 1):
-    """Run the oracle on the given rows of one plane in this process; returns (flops, seconds)."""
+def _oracle_units(w, x):
+    """(q_rows, k, v) fp32 arrays per unit of the workload, in plane order.
+
+    The fp32 arrays are exact images of the 16-bit inputs; the worker widens
+    them to fp64 (also exactly) before calling the oracle."""
+    def f32(t):
+        import torch
+        return t.detach().to(torch.float32).numpy()
+    units = []
+    if w.varlen is None:
+        for b in range(w.B):
+            for h in range(w.H):
+                units.append((x["q"][b, h], x["k"][b, h], x["v"][b, h]))
+    else:
+        cu = x["cu_seqlens"]
+        cuk = x["cu_seqlens_k"] if x["cu_seqlens_k"] is not None else cu
+        for s in range(len(cu) - 1):
+            for h in range(w.H):
+                units.append((x["q"][h, cu[s]:cu[s + 1]], x["k"][h, cuk[s]:cuk[s + 1]],
+                              x["v"][h, cuk[s]:cuk[s + 1]]))
+    out = []
+    for q, k, v in units:
+        r0 = max(0, q.shape[0] - UNIT_ROWS)
+        out.append((f32(q[r0:]), f32(k), f32(v)))
+    return out
+
+
+def _unit_flops(q, k, causal, D) -> float:
+    """FLOPs of one unit: 4 D per allowed (query, key) pair, the queries being
+    the last rows of the plane (key j allowed for query i when j <= i + Nk - Nq)."""
+    nq, nk = q.shape[0], k.shape[0]
+    if not causal:
+        return 4.0 * D * nq * nk
+    i = np.arange(nq)
+    return 4.0 * D * float(np.clip(i + 1 + (nk - nq), 0, nk).sum())
+
+
+def _oracle_unit(job):
+    """Worker: the oracle on one unit; returns its seconds in the worker."""
     import oracle
-    b, h = divmod(plane_index, w.H)
-    q = W.as_f64(x["q"][b, h])
-    k = W.as_f64(x["k"][b, h])
-    v = W.as_f64(x["v"][b, h])
-    with _blas_single_thread():
-        t0 = time.perf_counter()
-        oracle.attention_rows(q, k, v, w.scale, w.causal, rows)
-        dt = time.perf_counter() - t0
-    return _rows_flops(w, rows), dt
+    q, k, v, scale, causal = job
+    t0 = time.perf_counter()
+    oracle.attention_plane(q.astype(np.float64), k.astype(np.float64), v.astype(np.float64),
+                           scale, causal)
+    return time.perf_counter() - t0
 
 
-_ORACLE_PLANE = None
-
-
-def _oracle_worker_init(q, k, v, scale, causal):
-    global _ORACLE_PLANE
-    _ORACLE_PLANE = (q, k, v, scale, causal)
+def _oracle_worker_init():
     try:
         from threadpoolctl import threadpool_limits
         threadpool_limits(limits=1)
@@ -283,102 +318,89 @@ def _oracle_worker_init(q, k, v, scale, causal):
         pass
 
 
-def _oracle_worker_rows(rows):
-    import oracle
-    q, k, v, scale, causal = _ORACLE_PLANE
-    oracle.attention_rows(q, k, v, scale, causal, rows)
-    return len(rows)
-
-
 class OraclePool:
-    """The oracle on rows of one plane, row-parallel over spawned processes (one
-    BLAS thread each).  Processes, not threads: the per-row NumPy work is too
-    small to run in parallel under the interpreter lock.  Spawned, not forked:
-    a process forked after CUDA has been initialised can hang."""
+    """The oracle on whole planes, one plane per task, over `procs` spawned
+    processes with one BLAS thread each.  Spawned, not forked: a process forked
+    after CUDA has been initialised can hang.  procs == 1 runs in this process."""
 
-    def __init__(self, w, x, plane_index: int, procs: int):
-        import multiprocessing as mp
-        from concurrent.futures import ProcessPoolExecutor
-        b, h = divmod(plane_index, w.H)
-        init = (W.as_f64(x["q"][b, h]), W.as_f64(x["k"][b, h]), W.as_f64(x["v"][b, h]),
-                w.scale, w.causal)
-        self.w, self.x, self.plane, self.procs = w, x, plane_index, procs
-        self.ex = ProcessPoolExecutor(max_workers=procs, mp_context=mp.get_context("spawn"),
-                                      initializer=_oracle_worker_init, initargs=init)
-        # start every worker before anything is timed; a pool that does not come
-        # up (a worker that cannot start) falls back to this process alone
-        try:
-            list(self.ex.map(_oracle_worker_rows, [np.arange(1)] * (2 * procs), timeout=180))
-        except Exception:  # noqa: BLE001 - any failure: measure in-process instead
-            self.ex.shutdown(wait=False, cancel_futures=True)
-            self.ex, self.procs = None, 1
+    def __init__(self, w, units, procs: int):
+        self.w, self.units, self.procs, self.ex = w, units, procs, None
+        self.next = 0
+        if procs > 1:
+            import multiprocessing as mp
+            from concurrent.futures import ProcessPoolExecutor
+            self.ex = ProcessPoolExecutor(max_workers=procs, mp_context=mp.get_context("spawn"),
+                                          initializer=_oracle_worker_init)
+            # start every worker (and its imports) before anything is timed
+            tiny = (np.zeros((4, w.D), np.float32),) * 3
+            try:
+                list(self.ex.map(_oracle_unit, [tiny + (w.scale, w.causal)] * (2 * procs),
+                                 timeout=300))
+            except Exception:  # noqa: BLE001 - any failure: measure in-process instead
+                self.ex.shutdown(wait=False, cancel_futures=True)
+                self.ex, self.procs = None, 1
 
-    def run(self, rows: np.ndarray):
-        """(flops, seconds) of the oracle on `rows`, dealt round-robin so that
-        long and short causal rows spread evenly over the processes."""
-        if self.ex is None:
-            return oracle_rows_sample(self.w, self.x, self.plane, rows)
-        chunks = [rows[i::self.procs] for i in range(self.procs) if len(rows[i::self.procs])]
+    def round(self):
+        """One round: the next `procs` units (cycling over the workload), one per
+        process.  Returns (flops, wall seconds, units)."""
+        idx = [(self.next + i) % len(self.units) for i in range(self.procs)]
+        self.next = (self.next + self.procs) % len(self.units)
+        jobs = [self.units[i] + (self.w.scale, self.w.causal) for i in idx]
+        flops = sum(_unit_flops(j[0], j[1], self.w.causal, self.w.D) for j in jobs)
         t0 = time.perf_counter()
-        list(self.ex.map(_oracle_worker_rows, chunks, timeout=600))
-        return _rows_flops(self.w, rows), time.perf_counter() - t0
+        if self.ex is None:
+            with _blas_single_thread():
+                for j in jobs:
+                    _oracle_unit(j)
+        else:
+            list(self.ex.map(_oracle_unit, jobs, timeout=1800))
+        return flops, time.perf_counter() - t0, len(jobs)
 
     def close(self):
         if self.ex is not None:
             self.ex.shutdown()
 
 
-def _sample_block(n: int, done: int, size: int) -> np.ndarray:
-    """The next block of the sample: the plane's rows from the last one backwards
-    (the full-length causal rows first), starting over once all have been used."""
-    r1 = n - (done % n)
-    return np.arange(max(0, r1 - size), r1)
+def _unit_desc(w):
+    return (f"whole planes (the last {UNIT_ROWS} query rows of longer ones)" if w.varlen is None
+            else f"whole (sequence, head) planes (the last {UNIT_ROWS} rows of longer ones)")
 
 
-def cpu_baseline(w, x, budget_s: float = 12.0):
-    """Oracle throughput on a bounded sample: the last rows of plane 0 (full-length causal rows),
-    dealt over a process per core; if that turns out slower than one process (a host whose
-    cores are shared or throttled), one process on the same budget."""
+def cpu_baseline(w, x, cpu_seconds: float = 20.0):
+    """Oracle throughput on a bounded sample: rounds of one plane per process,
+    one process per core, until about `cpu_seconds` of CPU work; if that is
+    slower than one process (a host whose cores are shared or throttled), one
+    process on the same kind of sample."""
+    units = _oracle_units(w, x)
     procs = host_cores()
-    # the same oracle in one process, on the last 256 rows
-    one = np.arange(max(0, w.N - 256), w.N)
-    f1, dt1 = oracle_rows_sample(w, x, 0, one)
+    one = OraclePool(w, units, 1)
+    f1, dt1, _ = one.round()
     v1 = f1 / dt1 / 1e12
-    pool = OraclePool(w, x, 0, procs)
+    pool = OraclePool(w, units, procs)
+    flops = secs = 0.0
+    n = 0
     try:
-        n_rows = 256
-        flops_total, t_total, rows_done = 0.0, 0.0, 0
-        while t_total < budget_s:
-            rows = _sample_block(w.N, rows_done, n_rows)
-            f, dt = pool.run(rows)
-            flops_total += f
-            t_total += dt
-            rows_done += len(rows)
-            n_rows = min(16384, n_rows * 2)
+        while secs * pool.procs < cpu_seconds or n == 0:
+            f, dt, k = pool.round()
+            flops, secs, n = flops + f, secs + dt, n + k
     finally:
         pool.close()
-    procs = pool.procs
-    value = flops_total / t_total / 1e12
-    how = f"rows dealt over {procs} processes"
-    if procs > 1 and value < v1:
-        # more processes than the host really runs at once: one process instead
-        flops_total, t_total, rows_done, n_rows = 0.0, 0.0, 0, 256
-        while t_total < budget_s:
-            rows = _sample_block(w.N, rows_done, n_rows)
-            f, dt = oracle_rows_sample(w, x, 0, rows)
-            flops_total += f
-            t_total += dt
-            rows_done += len(rows)
-            n_rows = min(4096, n_rows * 2)
-        how = (f"one process ({procs} processes ran at {value:.2e} TFLOP/s, below one "
-               f"process: the host's cores are shared or throttled)")
-        value, procs = flops_total / t_total / 1e12, 1
-    return {"value": value, "unit": "TFLOP/s", "cores": procs,
-            "kind": "oracle", "value_1core": v1,
-            "sample": f"fp64 oracle on {rows_done} query rows of plane (b=0,h=0) of "
-                      f"{w.name} (from the last row backwards, starting over after row 0), "
-                      f"{how} ({t_total:.1f} s); "
-                      f"value_1core: the last {len(one)} rows in one process ({dt1:.2f} s)"}
+    value, used = flops / secs / 1e12, pool.procs
+    how = f"one plane per process, {used} processes"
+    if used > 1 and value < v1:
+        flops, secs, n = f1, dt1, 1
+        while secs < cpu_seconds:
+            f, dt, k = one.round()
+            flops, secs, n = flops + f, secs + dt, n + k
+        how = (f"one process ({used} processes ran at {value:.2e} TFLOP/s, below one process: "
+               f"the host's cores are shared or throttled)")
+        value, used = flops / secs / 1e12, 1
+    return {"value": value, "unit": "TFLOP/s", "cores": used, "kind": "oracle",
+            "value_1core": v1,
+            "sample": f"fp64 oracle.attention_plane on {n} {_unit_desc(w)} of {w.name}, "
+                      f"{how}, {secs:.1f} s wall; FLOPs counted as 4 D per allowed "
+                      f"(query, key) pair; value_1core: one plane in one process "
+                      f"({dt1:.2f} s)"}
 
 
 def run_reference(args, w):
@@ -386,22 +408,24 @@ def run_reference(args, w):
     if rank != 0:
         return 0
     x = W.generate(w)
-    threads = host_cores()
-    rows = np.arange(max(0, w.N - 512), w.N)   # one step: the last 512 rows of plane 0
-    pool = OraclePool(w, x, 0, threads)
+    units = _oracle_units(w, x)
+    pool = OraclePool(w, units, host_cores())
     try:
         # a process per core, unless that is slower than one process on this host
-        _, t_one = oracle_rows_sample(w, x, 0, rows)
-        _, t_pool = pool.run(rows)
-        step = pool.run if t_pool < t_one else (lambda r: oracle_rows_sample(w, x, 0, r))
-        threads = pool.procs if t_pool < t_one else 1
+        if pool.procs > 1:
+            one = OraclePool(w, units, 1)
+            f1, t1, _ = one.round()
+            fp, tp, _ = pool.round()
+            if fp / tp < f1 / t1:
+                pool.close()
+                pool = one
         for _ in range(args.warmup):
-            step(rows)
+            pool.round()
         flops = secs = 0.0
+        n = 0
         for _ in range(args.steps):
-            f, dt = step(rows)
-            flops += f
-            secs += dt
+            f, dt, k = pool.round()
+            flops, secs, n = flops + f, secs + dt, n + k
     finally:
         pool.close()
     value = flops / secs / 1e12
@@ -411,10 +435,10 @@ def run_reference(args, w):
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(w),
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": f"each step: fp64 oracle on query rows {rows[0]}..{rows[-1]} "
-                                   f"of plane (b=0,h=0) of {w.name}, dealt over {threads} "
-                                   f"process(es)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": pool.procs, "kind": "oracle",
+                         "sample": f"each step: fp64 oracle.attention_plane on {pool.procs} "
+                                   f"{_unit_desc(w)} of {w.name}, one per process "
+                                   f"({n} units in the timed steps)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -439,6 +463,288 @@ def workload_config(w):
 # CUDA path
 # ---------------------------------------------------------------------------
 
+def graph_step_ms(step, steps, stream, dev):
+    """Milliseconds per step of `steps` calls of step(stream) captured into one
+    CUDA graph and replayed (the same kernels back to back, without host
+    launch gaps); None when the capture is refused."""
+    g = capture_graph(step, steps, stream, dev)
+    if g is None:
+        return None
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def capture_graph(step, steps, stream, dev):
+    """`steps` calls of step(st) captured into one CUDA graph (replayed once to
+    check it), or None when the capture is refused."""
+    import torch
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            for _ in range(steps):
+                step(torch.cuda.current_stream(dev))
+        stream.wait_stream(cap)
+        g.replay()
+        torch.cuda.synchronize()
+        return g
+    except Exception as e:  # noqa: BLE001 - the caller falls back to eager timing
+        print(f"[bench] graph capture failed ({e})", file=sys.stderr)
+        return None
+
+
+def fits_in_l2(nbytes: float) -> bool:
+    """Inputs that (mostly) fit in the 126 MB L2 are flushed between launches."""
+    return nbytes <= 126e6
+
+
+def time_steps(call, steps, warmup, stream, dev, local, ws, flush_needed):
+    """Device time of `steps` calls of call(stream).
+
+    Inputs larger than L2: the K calls are captured into one CUDA graph and
+    its replay is timed with CUDA events on the launching stream (the kernels
+    back to back, without host launch gaps).  Inputs that fit in L2: a 256 MB
+    buffer is written before every call and each call's own events give its
+    time; the same K calls warm in L2 (one graph) are timed beside.
+    Returns (ms per step, how it was timed, clock summary, warm ms or None).
+    """
+    import torch
+    from exact_io_aware_107_b300 import device_error
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush_needed else None
+    for _ in range(warmup):
+        if flush is not None:
+            flush.zero_()
+        call(stream)
+    torch.cuda.synchronize()
+    if device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    graph = capture_graph(call, steps, stream, dev) if flush is None else None
+    barrier(ws)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            if graph is not None:
+                starts[0].record(stream)
+                graph.replay()
+                ends[0].record(stream)
+            else:
+                for i in range(steps):
+                    if flush is not None:
+                        flush.zero_()
+                    starts[i].record(stream)
+                    call(stream)
+                    ends[i].record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    if device_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    warm = None
+    if graph is not None:
+        ms, how = starts[0].elapsed_time(ends[0]) / steps, "one CUDA graph of the K steps"
+    else:
+        ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / steps
+        if flush is not None:
+            how = "per-launch CUDA events, L2 flushed (256 MB written) before each launch"
+            warm = graph_step_ms(call, steps, stream, dev)
+        else:
+            how = "per-launch CUDA events (graph capture refused)"
+    return ms, how, clk.summary(), warm
+
+
+def device_inputs(x, dev):
+    import torch
+    q, k, v = (t.to(dev) for t in (x["q"], x["k"], x["v"]))
+    cu = None if x["cu_seqlens"] is None else torch.as_tensor(x["cu_seqlens"]).to(dev)
+    cuk = None if x["cu_seqlens_k"] is None else torch.as_tensor(x["cu_seqlens_k"]).to(dev)
+    return q, k, v, cu, cuk
+
+
+def forward_call(w, q, k, v, cu, cuk):
+    """call(stream): one forward of the workload into fixed output buffers."""
+    import torch
+    from exact_io_aware_107_b300 import attention_forward
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+
+    def call(st):
+        attention_forward(q, k, v, causal=w.causal, scale=w.scale, cu_seqlens=cu, out=o, lse=lse,
+                          stream=st, cu_seqlens_k=cuk)
+    return call, o, lse
+
+
+def tensor_peak():
+    peak_tf, _, kind = load_peaks()
+    src = (f"{kind} cuBLAS bf16 burst (MEASURED_PEAKS.json)" if kind == "measured"
+           else "fallback 1.8 PFLOP/s")
+    return peak_tf, src
+
+
+def measure_forward(w, x, steps, warmup, dev, stream, local=0, ws=1):
+    q, k, v, cu, cuk = device_inputs(x, dev)
+    call, _, _ = forward_call(w, q, k, v, cu, cuk)
+    ms, how, clocks, warm = time_steps(call, steps, warmup, stream, dev, local, ws,
+                                       fits_in_l2(3 * w.hbm_bytes() / 4))
+    return ms, how, clocks, warm
+
+
+def measure_backward(w, x, steps, warmup, dev, stream, local=0):
+    """Device ms per backward (prep, main and dQ kernels) of workload w."""
+    import torch
+    from exact_io_aware_107_b300 import _binding, attention_backward, attention_forward
+    q, k, v, cu, cuk = device_inputs(x, dev)
+    rng = np.random.default_rng(1)
+    do = torch.from_numpy(rng.standard_normal(tuple(q.shape), dtype=np.float32)).to(q.dtype).to(dev)
+    o, lse = attention_forward(q, k, v, causal=w.causal, scale=w.scale, cu_seqlens=cu,
+                               cu_seqlens_k=cuk, stream=stream)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    rc, nbytes = _binding.attn_bwd_workspace_bytes(w.B, w.H, w.N, w.D, cu is not None)
+    assert rc == 0
+    wsb = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+
+    def call(st):
+        attention_backward(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, cu_seqlens=cu,
+                           cu_seqlens_k=cuk, dq=dq, dk=dk, dv=dv, workspace=wsb, stream=st)
+    return time_steps(call, steps, warmup, stream, dev, local, 1,
+                      fits_in_l2(5 * w.hbm_bytes() / 4))
+
+
+def decode_bytes(B, H, Nq, Nk, D) -> float:
+    """Algorithmic HBM bytes of one decode: K and V read once, Q read, O and LSE written."""
+    return 2.0 * B * H * Nk * D * 2 + 2.0 * B * H * Nq * D * 2 + B * H * Nq * 4
+
+
+def measure_decode(shape, steps, warmup, dev, stream, local=0):
+    import torch
+    from exact_io_aware_107_b300 import _binding, attention_decode
+    B, H, Nq, Nk, D = shape
+    rng = np.random.default_rng(0)
+
+    def draw(*sh):
+        return torch.from_numpy(rng.standard_normal(sh, dtype=np.float32)).to(torch.bfloat16)
+    q, k, v = (t.to(dev) for t in (draw(B, H, Nq, D), draw(B, H, Nk, D), draw(B, H, Nk, D)))
+    rc, nbytes = _binding.attn_decode_workspace_bytes(B, H, Nq, Nk, D)
+    assert rc == 0
+    wsb = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+
+    def call(st):
+        attention_decode(q, k, v, workspace=wsb, out=o, lse=lse, stream=st)
+    ms, how, clocks, _ = time_steps(call, steps, warmup, stream, dev, local, 1,
+                                    fits_in_l2(2 * B * H * Nk * D * 2))
+    return ms, how, clocks, nbytes
+
+
+_READ_GBS = {}
+
+
+def hbm_read_gbs(dev, stream):
+    """Read-only HBM bandwidth of this GPU (best of 5 streams over 4 GiB, far
+    larger than L2), through the library's read probe; cached per device."""
+    import torch
+    from exact_io_aware_107_b300 import _binding
+    key = str(dev)
+    if key not in _READ_GBS:
+        nbytes = 4 << 30
+        buf = torch.ones(nbytes // 4, dtype=torch.int32, device=dev)
+        out = torch.zeros(1, dtype=torch.int32, device=dev)
+        best = float("inf")
+        for i in range(6):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            rc = _binding.attn_hbm_read_probe(buf.data_ptr(), nbytes, out.data_ptr(),
+                                              stream.cuda_stream)
+            e1.record(stream)
+            assert rc == 0
+            torch.cuda.synchronize()
+            if i > 0:
+                best = min(best, e0.elapsed_time(e1))
+        _READ_GBS[key] = nbytes / (best * 1e-3) / 1e9
+        del buf
+    return _READ_GBS[key]
+
+
+def hbm_peak(dev, stream):
+    """The larger of the measured copy bandwidth and this GPU's read-only stream."""
+    _, copy_gbs, kind = load_peaks()
+    read = hbm_read_gbs(dev, stream)
+    return max(copy_gbs, read), {"copy_gbs": copy_gbs, "copy_source": f"{kind} (MEASURED_PEAKS.json)"
+                                 if kind == "measured" else "fallback", "read_gbs": read,
+                                 "read_source": "attn_hbm_read_probe over 4 GiB, best of 5, "
+                                                "this GPU, this run"}
+
+
+# The other workloads carried in the default line (the headline stays the
+# causal N=8192 D=128 forward): the D=64 non-causal forward (L2-flushed and
+# warm), the long peaked causal forward, the packed variable-length forward,
+# the backward on the headline shape and a KV-cache decode.
+EXTRA_FORWARD = ("bf16_b4_h16_n2048_d64", "bf16_causal_b1_h16_n32768_d128_peaked",
+                 "bf16_varlen_causal_h32_d128")
+EXTRA_DECODE = (8, 32, 1, 32768, 128)
+
+
+def extra_workloads(args, dev, stream, local):
+    import torch
+    peak_tf, _ = tensor_peak()
+    out = {}
+
+    def fwd_entry(w, ms, how, clocks, warm):
+        tf = w.flops() / (ms * 1e-3) / 1e12
+        e = {"value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "timing": how,
+             "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_tf,
+                          "unit": "TFLOP/s", "frac": tf / peak_tf},
+             "clocks": clocks, "flops_per_step": w.flops()}
+        if warm is not None:
+            wt = w.flops() / (warm * 1e-3) / 1e12
+            e["warm_l2"] = {"value": wt, "unit": "TFLOP/s", "ms_per_step": warm,
+                            "frac": wt / peak_tf, "timing": "one CUDA graph of the K steps, "
+                                                            "inputs in L2"}
+        return e
+
+    for name in EXTRA_FORWARD:
+        w = W.WORKLOADS[name]
+        x = W.generate(w)
+        ms, how, clocks, warm = measure_forward(w, x, args.steps, args.warmup, dev, stream, local)
+        out[name] = fwd_entry(w, ms, how, clocks, warm)
+        del x
+        torch.cuda.empty_cache()
+    w = W.WORKLOADS[W.HEADLINE]
+    x = W.generate(w)
+    ms, how, clocks, _ = measure_backward(w, x, args.steps, args.warmup, dev, stream, local)
+    tf = 2.5 * w.flops() / (ms * 1e-3) / 1e12
+    out["backward_" + w.name] = {
+        "value": tf, "unit": "TFLOP/s (2.5x the forward's FLOPs)", "ms_per_step": ms,
+        "timing": how, "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_tf,
+                                    "unit": "TFLOP/s", "frac": tf / peak_tf},
+        "clocks": clocks, "kernels": "attn_bwd_prep_kernel, attn_bwd_bf16_kernel<128>, "
+                                      "attn_bwd_dq_kernel"}
+    del x
+    torch.cuda.empty_cache()
+    B, H, Nq, Nk, D = EXTRA_DECODE
+    ms, how, clocks, _ = measure_decode(EXTRA_DECODE, args.steps, args.warmup, dev, stream, local)
+    nb = decode_bytes(B, H, Nq, Nk, D)
+    gbs = nb / (ms * 1e-3) / 1e9
+    peak, src = hbm_peak(dev, stream)
+    out[f"decode_b{B}_h{H}_nq{Nq}_nk{Nk}_d{D}"] = {
+        "value": gbs, "unit": "GB/s", "ms_per_step": ms, "timing": how,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                     "frac": gbs / peak, "peak_source": src, "algorithmic_bytes": nb},
+        "clocks": clocks}
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, w):
     import torch
     from exact_io_aware_107_b300 import _binding, attention_forward, device_error
@@ -451,102 +757,23 @@ def run_ours(args, w):
     _binding.load()
     x = W.generate(w)
     dev = torch.device("cuda", local)
-    q, k, v = (t.to(dev) for t in (x["q"], x["k"], x["v"]))
-    cu = None if x["cu_seqlens"] is None else torch.as_tensor(x["cu_seqlens"]).to(dev)
-    cuk = None if x["cu_seqlens_k"] is None else torch.as_tensor(x["cu_seqlens_k"]).to(dev)
-    o = torch.empty_like(q)
-    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    flush = None
-    if 3 * w.hbm_bytes() / 4 <= 126e6:
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-
-    def step():
-        if flush is not None:
-            flush.zero_()
-        attention_forward(q, k, v, causal=w.causal, scale=w.scale, cu_seqlens=cu, out=o, lse=lse,
-                          stream=stream, cu_seqlens_k=cuk)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if device_error() != 0:
-        raise RuntimeError("device error during warm-up")
 
     # --- device-timed region (inputs resident) ---
-    # Without a flush the K steps are also captured into one CUDA graph and the
-    # graph's replay is what `value` times: the same kernels back to back, with
-    # no host launch gaps in between.
-    graph = None
-    if flush is None:
-        try:
-            graph = torch.cuda.CUDAGraph()
-            cap = torch.cuda.Stream(dev)
-            cap.wait_stream(stream)
-            with torch.cuda.graph(graph, stream=cap):
-                for _ in range(args.steps):
-                    attention_forward(q, k, v, causal=w.causal, scale=w.scale, cu_seqlens=cu,
-                                      out=o, lse=lse, cu_seqlens_k=cuk)
-            stream.wait_stream(cap)
-            graph.replay()
-            torch.cuda.synchronize()
-        except Exception as e:  # noqa: BLE001 - fall back to the eager region
-            print(f"[bench] graph capture failed ({e}); timing the eager launches", file=sys.stderr)
-            graph = None
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier(ws)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for i in range(args.steps):
-            if flush is not None:
-                flush.zero_()
-            starts[i].record(stream)
-            attention_forward(q, k, v, causal=w.causal, scale=w.scale, cu_seqlens=cu, out=o,
-                              lse=lse, stream=stream, cu_seqlens_k=cuk)
-            ends[i].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize()
-        if graph is not None:
-            g0 = torch.cuda.Event(enable_timing=True)
-            g1 = torch.cuda.Event(enable_timing=True)
-            barrier(ws)
-            with torch.cuda.stream(stream):
-                g0.record(stream)
-                graph.replay()
-                g1.record(stream)
-            torch.cuda.synchronize()
-    barrier(ws)
-    if device_error() != 0:
-        raise RuntimeError("device error in the timed region")
-    total_ms = t_start.elapsed_time(t_end)
-    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    kernel_ms = sum(launch_ms) / len(launch_ms)
-    # with an L2 flush between launches the step is the attention call alone
-    # (the events bracket it); otherwise the K steps of the graph replay
-    warm = None
-    if flush is not None:
-        step_ms, timing = kernel_ms, "per-launch CUDA events, L2 flushed between launches"
-        # the same workload warm in L2: the K steps back to back in one CUDA graph
-        warm_ms = graph_step_ms(
-            lambda st: attention_forward(q, k, v, causal=w.causal, scale=w.scale, cu_seqlens=cu,
-                                         out=o, lse=lse, stream=st, cu_seqlens_k=cuk),
-            args.steps, stream, dev)
-        if warm_ms is not None:
-            warm = {"value": w.flops() / (warm_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                    "ms_per_step": warm_ms, "timing": "one CUDA graph of the K steps, inputs in L2"}
-    elif graph is not None:
-        step_ms, timing = g0.elapsed_time(g1) / args.steps, "one CUDA graph of the K steps"
-    else:
-        step_ms, timing = total_ms / args.steps, "K eager launches back to back"
+    step_ms, timing, clocks, warm_ms = measure_forward(w, x, args.steps, args.warmup, dev, stream,
+                                                       local, ws)
     ms_step = max_over_ranks(step_ms, ws)
     flops = w.flops()
     value = ws * flops / (ms_step * 1e-3) / 1e12
+    # the dominant (and only) kernel of a step: its time per launch is the
+    # step's own device time on this rank
+    achieved = flops / (step_ms * 1e-3) / 1e12
+    torch.cuda.empty_cache()
 
     # --- end-to-end region: pinned host buffers, copies inside the timed region ---
+    q, k, v, cu, cuk = device_inputs(x, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
     hq, hk, hv = (t.pin_memory() for t in (x["q"], x["k"], x["v"]))
     ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
@@ -589,11 +816,12 @@ def run_ours(args, w):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, ws)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    del q, k, v, o, lse
+    torch.cuda.empty_cache()
 
-    peak_tf, _, peak_kind = load_peaks()
-    achieved = flops / (kernel_ms * 1e-3) / 1e12
-    print(f"[bench] {w.name}: {ms_step:.3f} ms/step, {value:.1f} TFLOP/s, kernel {kernel_ms:.3f} ms"
-          f" ({achieved:.1f} TFLOP/s), e2e {e2e_ms:.3f} ms", file=sys.stderr)
+    peak_tf, peak_src = tensor_peak()
+    print(f"[bench] {w.name}: {ms_step:.3f} ms/step, {value:.1f} TFLOP/s ({timing}), "
+          f"e2e {e2e_ms:.3f} ms", file=sys.stderr)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -601,25 +829,29 @@ def run_ours(args, w):
         "data": "synthetic", "config": {**workload_config(w), "timing": timing},
         "pct_of_peak": 100.0 * value / ws / peak_tf,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf,
-                     "unit": "TFLOP/s", "frac": achieved / peak_tf,
-                     "peak_source": f"{peak_kind} cuBLAS bf16 burst (MEASURED_PEAKS.json)"
-                     if peak_kind == "measured" else "fallback 1.8 PFLOP/s",
+                     "unit": "TFLOP/s", "frac": achieved / peak_tf, "peak_source": peak_src,
                      "kernel": f"attn_fwd_bf16_kernel<{w.D}>",
+                     "kernel_time": f"{step_ms:.4f} ms per launch ({timing}; the step is this "
+                                    f"one kernel)",
                      "traffic": measured_traffic(w.name),
                      "algorithmic_bytes": w.hbm_bytes(),
-                     "algorithmic_gbs": w.hbm_bytes() / (kernel_ms * 1e-3) / 1e9},
+                     "algorithmic_gbs": w.hbm_bytes() / (step_ms * 1e-3) / 1e9},
         "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "call": "attn_fwd_host (pinned host buffers; chunked copies overlapped with the "
                         "kernels)" if host_api else
                         "attn_fwd after pinned host-to-device copies, results copied back"},
         "gpu_launches": args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "gpu": torch.cuda.get_device_name(dev),
         "system": system_info(dev),
     }
-    if warm is not None:
-        line["warm_l2"] = warm
+    if warm_ms is not None:
+        wt = flops / (warm_ms * 1e-3) / 1e12
+        line["warm_l2"] = {"value": wt, "unit": "TFLOP/s", "ms_per_step": warm_ms,
+                           "timing": "one CUDA graph of the K steps, inputs in L2"}
+    if rank == 0 and not args.no_extra:
+        line["workloads"] = extra_workloads(args, dev, stream, local)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, x)
     if rank == 0:
@@ -630,101 +862,34 @@ def run_ours(args, w):
     return 0
 
 
-def graph_step_ms(step, steps, stream, dev):
-    """Milliseconds per step of `steps` calls of step() captured into one CUDA
-    graph and replayed (the same kernels back to back, without host launch
-    gaps); None when the capture is refused."""
-    import torch
-    try:
-        g = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        with torch.cuda.graph(g, stream=cap):
-            for _ in range(steps):
-                step(torch.cuda.current_stream(dev))
-        stream.wait_stream(cap)
-        g.replay()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / steps
-    except Exception as e:  # noqa: BLE001 - the caller falls back to eager timing
-        print(f"[bench] graph capture failed ({e})", file=sys.stderr)
-        return None
-
-
 def run_backward(args, w):
-    """Backward pass (a NEXT row): device-timed TFLOP/s, 2.5x the forward's FLOPs
+    """Backward pass alone: device-timed TFLOP/s, 2.5x the forward's FLOPs
     (five matrix products per tile pair instead of two)."""
     import torch
-    from exact_io_aware_107_b300 import (_binding, attention_backward, attention_forward,
-                                         device_error)
-
+    from exact_io_aware_107_b300 import _binding
     _, _, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     _binding.load()
     x = W.generate(w)
-    q, k, v = (t.to(dev) for t in (x["q"], x["k"], x["v"]))
-    rng = np.random.default_rng(1)
-    do = torch.from_numpy(rng.standard_normal(tuple(q.shape), dtype=np.float32)).to(q.dtype).to(dev)
-    cu = None if x["cu_seqlens"] is None else torch.as_tensor(x["cu_seqlens"]).to(dev)
-    cuk = None if x["cu_seqlens_k"] is None else torch.as_tensor(x["cu_seqlens_k"]).to(dev)
     stream = torch.cuda.current_stream(dev)
-    o, lse = attention_forward(q, k, v, causal=w.causal, scale=w.scale, cu_seqlens=cu,
-                               cu_seqlens_k=cuk, stream=stream)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    rc, nbytes = _binding.attn_bwd_workspace_bytes(w.B, w.H, w.N, w.D, cu is not None)
-    assert rc == 0
-    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
-
-    def step(st=stream):
-        attention_backward(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, cu_seqlens=cu,
-                           cu_seqlens_k=cuk, dq=dq, dk=dk, dv=dv, workspace=ws, stream=st)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if device_error() != 0:
-        raise RuntimeError("device error during warm-up")
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    with ClockSampler(local) as clk:
-        for i in range(args.steps):
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        torch.cuda.synchronize()
-        g_ms = graph_step_ms(step, args.steps, stream, dev)
-    if device_error() != 0:
-        raise RuntimeError("device error in the timed region")
-    eager_ms = sum(s_.elapsed_time(e) for s_, e in zip(starts, ends)) / args.steps
-    ms = g_ms if g_ms is not None else eager_ms
+    ms, how, clocks, _ = measure_backward(w, x, args.steps, args.warmup, dev, stream, local)
     flops = 2.5 * w.flops()
-    peak_tf, _, peak_kind = load_peaks()
+    peak_tf, peak_src = tensor_peak()
     tf = flops / (ms * 1e-3) / 1e12
     print(f"[bench] backward {w.name}: {ms:.3f} ms/step, {tf:.1f} TFLOP/s", file=sys.stderr)
     line = {
         "metric": "attention bwd TFLOPS (bf16, 2.5x forward FLOPs)", "value": tf,
         "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
-        "config": {**workload_config(w),
-                   "l2": "inputs larger than L2 (no flush)" if 5 * w.hbm_bytes() / 4 > 126e6
-                   else "inputs smaller than L2 (not flushed)",
-                   "timing": "one CUDA graph of the K steps" if g_ms is not None
-                   else "per-step CUDA events"},
+        "dtype": w.dtype, "data": "synthetic",
+        "config": {**workload_config(w), "timing": how},
         "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": tf / peak_tf, "peak_source": f"{peak_kind} cuBLAS bf16 burst",
+                     "frac": tf / peak_tf, "peak_source": peak_src,
                      "kernel": f"attn_bwd_bf16_kernel<{w.D}> (+ prep and dQ kernels)",
                      "traffic": None},
         "gpu_launches": 3 * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "gpu": torch.cuda.get_device_name(dev), "system": system_info(dev),
     }
     print(json.dumps(line))
@@ -732,62 +897,33 @@ def run_backward(args, w):
 
 
 def run_decode(args):
-    """KV-cache decode (a NEXT row): device-timed GB/s against the HBM roofline."""
+    """KV-cache decode alone: device-timed GB/s against the HBM read roofline."""
     import torch
-    from exact_io_aware_107_b300 import _binding, attention_decode, device_error
-
-    ws_, rank, local = dist_env()
+    from exact_io_aware_107_b300 import _binding
+    _, _, local = dist_env()
     torch.cuda.set_device(local)
-    B, H, Nq, Nk, D = (int(t) for t in args.decode_shape.split(","))
-    rng = np.random.default_rng(0)
-    def draw(*shape):
-        return torch.from_numpy(rng.standard_normal(shape, dtype=np.float32)).to(torch.bfloat16)
-    q, k, v = draw(B, H, Nq, D), draw(B, H, Nk, D), draw(B, H, Nk, D)
     dev = torch.device("cuda", local)
-    dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
-    rc, nbytes = _binding.attn_decode_workspace_bytes(B, H, Nq, Nk, D)
-    assert rc == 0
-    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
-    o = torch.empty_like(dq)
-    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    _binding.load()
     stream = torch.cuda.current_stream(dev)
-    for _ in range(args.warmup):
-        attention_decode(dq, dk, dv, workspace=ws, out=o, lse=lse, stream=stream)
-    torch.cuda.synchronize()
-    assert device_error() == 0
-    with ClockSampler(local) as clk:
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            attention_decode(dq, dk, dv, workspace=ws, out=o, lse=lse, stream=stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        g_ms = graph_step_ms(lambda st: attention_decode(dq, dk, dv, workspace=ws, out=o, lse=lse,
-                                                         stream=st),
-                             args.steps, stream, dev)
-    assert device_error() == 0
-    ms = g_ms if g_ms is not None else e0.elapsed_time(e1) / args.steps
-    nbytes_alg = 2 * B * H * Nk * D * 2 + 2 * B * H * Nq * D * 2 + B * H * Nq * 4
-    _, hbm_peak, kind = load_peaks()
-    gbs = nbytes_alg / (ms * 1e-3) / 1e9
+    shape = tuple(int(t) for t in args.decode_shape.split(","))
+    B, H, Nq, Nk, D = shape
+    ms, how, clocks, nbytes = measure_decode(shape, args.steps, args.warmup, dev, stream, local)
+    nb = decode_bytes(B, H, Nq, Nk, D)
+    gbs = nb / (ms * 1e-3) / 1e9
+    peak, src = hbm_peak(dev, stream)
     line = {
         "metric": "attention decode GB/s (bf16, KV cache, non-causal)", "value": gbs,
         "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"decode_b{B}_h{H}_nq{Nq}_nk{Nk}_d{D}", "B": B, "H": H, "Nq": Nq,
-                   "Nk": Nk, "D": D, "workspace_bytes": nbytes,
-                   "timing": "one CUDA graph of the K steps" if g_ms is not None
-                   else "K launches back to back",
-                   "l2": "K/V larger than L2 (no flush)" if 2 * B * H * Nk * D * 2 > 126e6
-                   else "K/V fit in L2"},
-        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": gbs / hbm_peak, "peak_source": f"{kind} copy bandwidth",
+                   "Nk": Nk, "D": D, "workspace_bytes": nbytes, "timing": how},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                     "frac": gbs / peak, "peak_source": src,
                      "kernel": f"attn_decode_bf16_kernel<{D}>", "traffic": None,
-                     "algorithmic_bytes": nbytes_alg},
+                     "algorithmic_bytes": nb},
         "gpu_launches": args.steps * (2 if nbytes > 0 else 1),
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "gpu": torch.cuda.get_device_name(dev), "system": system_info(dev),
     }
     print(json.dumps(line))
@@ -803,6 +939,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=W.HEADLINE,
                     choices=sorted(W.WORKLOADS) + sorted(W.CROSS_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="leave out the other workloads (key 'workloads' of the line)")
     ap.add_argument("--op", choices=["forward", "backward", "decode"], default="forward",
                     help="backward: dQ, dK, dV (TFLOP/s); decode: the KV-cache decode path "
                          "(GB/s against HBM)")

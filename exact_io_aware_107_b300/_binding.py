@@ -64,7 +64,10 @@ _SIGNATURES = {
     "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_get_device_error": (ctypes.c_int, [ctypes.c_void_p]),
     "attn_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_ulonglong]),
+    "attn_set_fault_injection": (ctypes.c_int, [ctypes.c_int]),
     "attn_wait_selftest": (ctypes.c_int, [ctypes.c_ulonglong, ctypes.c_void_p]),
+    "attn_hbm_read_probe": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_void_p,
+                                           ctypes.c_void_p]),
     "attn_version": (ctypes.c_int, []),
 }
 
@@ -186,8 +189,17 @@ def attn_set_wait_timeout_ns(ns: int) -> int:
     return load().attn_set_wait_timeout_ns(int(ns))
 
 
+def attn_set_fault_injection(on: int) -> int:
+    return load().attn_set_fault_injection(int(on))
+
+
 def attn_wait_selftest(timeout_ns: int, stream) -> int:
     return load().attn_wait_selftest(int(timeout_ns), stream)
+
+
+def attn_hbm_read_probe(buf, nbytes, out, stream) -> int:
+    """Read-only stream over `nbytes` of device memory (bandwidth measurement)."""
+    return load().attn_hbm_read_probe(buf, int(nbytes), out, stream)
 
 
 def attn_version() -> int:

@@ -33,6 +33,10 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::atomic<unsigned long long> g_timeout_ns{1000000000ull};
+// Smallest wait budget attn_set_wait_timeout_ns accepts.
+constexpr unsigned long long kMinTimeoutNs = 1000000ull;
+// Set by attn_set_fault_injection: launches made while it is on stall CTA 0.
+std::atomic<int> g_stall{0};
 
 struct DeviceState {
   int checked = 0;  // 0 unknown, 1 ok, -1 wrong arch
@@ -208,6 +212,30 @@ __global__ void wait_selftest_kernel(unsigned long long budget, unsigned int* er
 
 
 
+// Read-only stream of device memory (a measurement helper): every thread reads
+// 16-byte words that skip L1, four loads in flight, and folds them with XOR;
+// each warp folds its lanes and XORs one word into *out, so no load is dead.
+__global__ void __launch_bounds__(512)
+    hbm_read_probe_kernel(const uint4* __restrict__ p, unsigned long long n16,
+                          unsigned int* out) {
+  const unsigned long long stride = static_cast<unsigned long long>(gridDim.x) * blockDim.x;
+  unsigned long long i = static_cast<unsigned long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  uint32_t acc = 0;
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    const uint4 a = __ldg(p + i), b = __ldg(p + i + stride), c = __ldg(p + i + 2 * stride),
+                d = __ldg(p + i + 3 * stride);
+    acc ^= a.x ^ a.y ^ a.z ^ a.w ^ b.x ^ b.y ^ b.z ^ b.w ^ c.x ^ c.y ^ c.z ^ c.w ^ d.x ^ d.y ^
+           d.z ^ d.w;
+  }
+  for (; i < n16; i += stride) {
+    const uint4 a = __ldg(p + i);
+    acc ^= a.x ^ a.y ^ a.z ^ a.w;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) atomicXor(out, acc);
+}
+
 // 16-bit (bf16 or fp16) forward on the tcgen05 kernel.
 int fwd_16bit(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
               int Nq, int Nk, int D, const int* cu_q, const int* cu_k, int causal, float scale,
@@ -248,6 +276,7 @@ int fwd_16bit(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.n_tiles = static_cast<int>(tiles);
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.stall = g_stall.load();
   p.timeout_ns = g_timeout_ns.load();
   p.err = st->err;
 
@@ -433,6 +462,7 @@ int bwd_16bit(const void* q, const void* k, const void* v, const void* o, const 
   p.causal = causal ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.stall = g_stall.load();
   p.timeout_ns = g_timeout_ns.load();
   p.err = st->err;
   const unsigned g = static_cast<unsigned>(grid);
@@ -507,6 +537,7 @@ int launch_decode(const void* q, const void* k, const void* v, void* o, float* l
   p.nsplit = plan.nsplit;
   p.chunk = plan.chunk;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.stall = g_stall.load();
   p.timeout_ns = g_timeout_ns.load();
   p.err = st->err;
   const unsigned grid = static_cast<unsigned>(planes * plan.nsplit);
@@ -534,6 +565,8 @@ extern "C" int attn_decode_workspace_bytes(int B, int H, int Nq, int Nk, int D,
   if (!bytes) return ATTN_ERR_NULL;
   if (B < 1 || H < 1 || Nq < 1 || Nq > kDecodeMaxQ || Nk < 1) return ATTN_ERR_SHAPE;
   if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+  // the plane limit of the decode entry points (B * H is then an int)
+  if (1LL * B * H > (1 << 24)) return ATTN_ERR_SHAPE;
   DeviceState* st = nullptr;
   const int rc = prepare_device(&st);
   if (rc != ATTN_OK) return rc;
@@ -854,8 +887,14 @@ extern "C" int attn_get_device_error(void* stream) {
 }
 
 extern "C" int attn_set_wait_timeout_ns(unsigned long long ns) {
-  if (ns == 0) return ATTN_ERR_SHAPE;
+  if (ns < kMinTimeoutNs) return ATTN_ERR_SHAPE;
   g_timeout_ns.store(ns);
+  return ATTN_OK;
+}
+
+extern "C" int attn_set_fault_injection(int on) {
+  if (on != 0 && on != 1) return ATTN_ERR_SHAPE;
+  g_stall.store(on);
   return ATTN_OK;
 }
 
@@ -868,4 +907,17 @@ extern "C" int attn_wait_selftest(unsigned long long timeout_ns, void* stream) {
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
-extern "C" int attn_version(void) { return 200; }
+extern "C" int attn_hbm_read_probe(const void* buf, unsigned long long bytes, unsigned int* out,
+                                   void* stream) {
+  if (!buf || !out) return ATTN_ERR_NULL;
+  if (bytes == 0 || bytes % 16 != 0) return ATTN_ERR_SHAPE;
+  if (!aligned(buf, 16) || !aligned(out, 4)) return ATTN_ERR_ALIGN;
+  DeviceState* st = nullptr;
+  const int rc = prepare_device(&st);
+  if (rc != ATTN_OK) return rc;
+  hbm_read_probe_kernel<<<4 * st->sms, 512, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(buf), bytes / 16, out);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+extern "C" int attn_version(void) { return 201; }

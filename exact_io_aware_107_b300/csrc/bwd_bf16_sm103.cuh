@@ -106,6 +106,7 @@ struct BwdParams {
   int causal;
   float scale;
   float scale_log2;         // scale * log2(e)
+  int stall;                // abort-path test: CTA 0 waits on a phase nothing completes
   unsigned long long timeout_ns;
   unsigned int* err;
 };
@@ -519,7 +520,10 @@ __global__ void __launch_bounds__(448, 1)
                                          1024)};
     const uint32_t tS = tmem + C::S_COL, tDP = tmem + C::DP_COL;
     const uint32_t tDV = tmem + C::DV_COL, tDK = tmem + C::DK_COL;
-    bool ok = wait(kv_full, 0) && wait(&q_full[0], 0);
+    // abort-path test: mma_done completes only after this warp's own final
+    // commit, so this wait runs out of budget and the whole CTA aborts
+    bool ok = (!p.stall || blockIdx.x != 0 || wait(mma_done, 0)) && wait(kv_full, 0) &&
+              wait(&q_full[0], 0);
     if (ok) {
       tc_fence_after();
       bwd_mma_kk<D>(tS, kA, qK[0], id_s, 0);  // S_0^T = K Q_0^T

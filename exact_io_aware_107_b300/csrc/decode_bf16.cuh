@@ -41,6 +41,7 @@ struct DecodeParams {
   int nsplit;       // key slices per plane
   int chunk;        // keys per slice (a multiple of 128)
   float scale_log2;
+  int stall;        // abort-path test: CTA 0 waits on a phase nothing completes
   unsigned long long timeout_ns;
   unsigned int* err;
 };
@@ -293,7 +294,11 @@ __global__ void __launch_bounds__(288)
   if (warp == C::WARPS) {
     // ------------------------------------------------------------ TMA producer
     int t = 0;
-    for (; t < ntiles; ++t) {
+    // abort-path test: empty[0] completes only once tile 0 (not loaded yet)
+    // has been read, so this wait runs out of budget and the CTA aborts
+    const bool stalled = p.stall && blockIdx.x == 0 &&
+                         !__all_sync(0xffffffffu, mbar_wait(&empty[0], 0, ctl));
+    for (; !stalled && t < ntiles; ++t) {
       const int s = t % NS, u = t / NS;
       if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(&empty[s], (u - 1) & 1, ctl))) break;
       mbar_arrive_expect_tx_warp(&full[s], 2 * C::TILE_BYTES);

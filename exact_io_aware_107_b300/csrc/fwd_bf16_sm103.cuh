@@ -70,6 +70,7 @@ struct Bf16Params {
   int n_tiles;            // packed: an upper bound on the work tiles
   int causal;
   float scale_log2;       // scale * log2(e)
+  int stall;              // abort-path test: CTA 0 waits on a phase nothing completes
   unsigned long long timeout_ns;
   unsigned int* err;
 };
@@ -458,6 +459,9 @@ __global__ void __launch_bounds__(320, 1)
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl));
     };
+    // abort-path test: mma_done completes only after this warp's own final
+    // commit, so this wait runs out of budget and the whole CTA aborts
+    if (p.stall && blockIdx.x == 0) ok = wait(mma_done, 0);
     for (int it = 0; ok; ++it) {
       const int step = bf16_tile(p, it, cur, w);
       if (step == kTileEnd) break;

@@ -82,13 +82,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// Lower bound of a drain wait, whatever budget the caller set for the other
+// waits.  A drain waits for copies and MMAs that were already issued, which
+// end within microseconds on a working GPU; the CTA may not free its tensor
+// memory or exit before they have, so a short user budget must not cut it.
+constexpr unsigned long long kDrainFloorNs = 1000000000ull;
+
 // Wait that ignores the abort flag (used during teardown to drain work that
-// is already in flight); bounded by the same budget.
+// is already in flight); bounded by the larger of the budget and the floor.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
   const uint32_t a = smem_u32(bar);
   const uint64_t t0 = global_timer_ns();
+  const uint64_t limit = c.budget > kDrainFloorNs ? c.budget : kDrainFloorNs;
   while (!mbar_try_wait(a, parity)) {
-    if (global_timer_ns() - t0 > c.budget) {
+    if (global_timer_ns() - t0 > limit) {
       atomicOr(c.err, kDevErrTimeout);
       return false;
     }

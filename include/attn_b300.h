@@ -269,10 +269,30 @@ int attn_get_device_error(void* stream);
 
 /*
  * Budget, in nanoseconds of GPU global time, of every bounded wait inside
- * the kernels launched after this call (default 1e9 = one second).  Returns
- * ATTN_ERR_SHAPE for 0.
+ * the kernels launched after this call (default 1e9 = one second).  The
+ * budget must exceed the longest wait a launch legitimately makes (a role
+ * can wait for a whole query tile of another role, which grows with the
+ * sequence length).  Returns ATTN_ERR_SHAPE below 1e6 (one millisecond).
+ * A kernel whose wait ran out still waits for the copies and MMAs it has
+ * already issued before it frees its tensor memory and exits; those drain
+ * waits are bounded by the larger of this budget and one second, whatever
+ * the budget.
  */
 int attn_set_wait_timeout_ns(unsigned long long ns);
+
+/*
+ * Abort-path test switch (on = 1, off = 0; anything else returns
+ * ATTN_ERR_SHAPE).  While it is on, every launch of the forward, backward and
+ * decode kernels makes its first thread block wait on an mbarrier phase
+ * that nothing completes: that wait runs out of budget, the block raises its
+ * abort flag, its other roles stop waiting, in-flight copies and MMAs
+ * drain, tensor memory is freed and the block exits.  The call then reports
+ * ATTN_ERR_TIMEOUT through attn_get_device_error, and its outputs are
+ * undefined.  Nothing traps and the context stays usable.  It exists so that
+ * tests can exercise the real kernels' timeout path; keep it off otherwise.
+ * It applies to launches made after the call, from any thread.
+ */
+int attn_set_fault_injection(int on);
 
 /*
  * Launches one CTA that waits on an mbarrier no thread ever arrives on, with
@@ -282,6 +302,20 @@ int attn_set_wait_timeout_ns(unsigned long long ns);
  * usable.  Asynchronous like the other calls.
  */
 int attn_wait_selftest(unsigned long long timeout_ns, void* stream);
+
+/*
+ * Measurement helper, not an attention operation (the pages have no
+ * counterpart): reads `bytes` of device memory at `buf` once, as a
+ * read-only stream (16-byte loads that skip L1, 4 x SM-count blocks of 512
+ * threads), and XORs a fold of the data into the device word *out.  Timed
+ * with CUDA events around it on `stream`, bytes / time is the read bandwidth
+ * that bounds kernels which only read HBM (the KV-cache decode); a copy moves
+ * twice the bytes and reaches a lower figure.  buf 16-byte aligned, bytes a
+ * positive multiple of 16, out 4-byte aligned device memory (its prior value
+ * is XORed into, not replaced).  Asynchronous; allocates nothing.
+ */
+int attn_hbm_read_probe(const void* buf, unsigned long long bytes, unsigned int* out,
+                        void* stream);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int attn_version(void);

@@ -42,11 +42,43 @@ def test_version_and_strerror(lib):
     assert B.strerror(-1234) == "unknown status"
 
 
-P = 1 << 20  # a 16-byte aligned stand-in address; never dereferenced on these paths
+BUF_BYTES = 8 << 20
+
+
+@pytest.fixture(scope="module")
+def buffers():
+    """Addresses for the argument-error cases, inside buffers this module owns.
+
+    Every shape these tests pass fits in BUF_BYTES, so a call that got past
+    its checks by mistake would still only touch memory it may touch.  With a
+    CUDA device the device address is a real device allocation; without one
+    no call can launch, and a host buffer serves for both.
+    """
+    import numpy as np
+    import torch
+    host = np.zeros(BUF_BYTES + 256, dtype=np.uint8)
+    hp = (host.ctypes.data + 255) // 256 * 256
+    dev = torch.zeros(BUF_BYTES, dtype=torch.uint8, device="cuda") \
+        if torch.cuda.is_available() else None
+    yield (dev.data_ptr() if dev is not None else hp), hp
+    if dev is not None:
+        torch.cuda.synchronize()
+
+
+@pytest.fixture
+def P(buffers):
+    """A 256-byte aligned device address (see `buffers`)."""
+    return buffers[0]
+
+
+@pytest.fixture
+def HP(buffers):
+    """A 256-byte aligned host address (see `buffers`)."""
+    return buffers[1]
 
 
 @pytest.mark.parametrize("fn", [B.attn_fwd, B.attn_fwd_f16, B.attn_fwd_f32])
-def test_argument_errors_return_before_launch(lib, fn):
+def test_argument_errors_return_before_launch(lib, fn, P):
     good = dict(q=P, k=P, v=P, o=P, lse=P, B=1, H=1, N=16, D=64, cu_seqlens=None, causal=1,
                 scale=0.125, stream=None)
 
@@ -74,7 +106,7 @@ def test_argument_errors_return_before_launch(lib, fn):
 
 
 @pytest.mark.parametrize("dtype", [B.ATTN_BF16, B.ATTN_F16, B.ATTN_F32])
-def test_cross_argument_errors(lib, dtype):
+def test_cross_argument_errors(lib, dtype, P):
     def call(**kw):
         a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, H=2, Nq=16, Nk=40, D=64, cq=None, ck=None,
                  causal=1, scale=0.125, dtype=dtype)
@@ -100,10 +132,11 @@ def test_cross_argument_errors(lib, dtype):
     assert call(Nk=0, k=None, v=None) in (B.ATTN_OK, B.ATTN_ERR_LAUNCH)
 
 
-def test_host_forward_argument_errors(lib):
+def test_host_forward_argument_errors(lib, P, HP):
+    # q, k, v, o, lse are host addresses here, the workspace a device address
     def call(**kw):
-        a = dict(q=P, k=P, v=P, o=P, lse=P, B=2, H=3, N=100, D=128, causal=1, scale=0.1,
-                 dtype=B.ATTN_BF16, ws=P, wsb=1 << 30)
+        a = dict(q=HP, k=HP, v=HP, o=HP, lse=HP, B=2, H=3, N=100, D=128, causal=1, scale=0.1,
+                 dtype=B.ATTN_BF16, ws=P, wsb=BUF_BYTES)
         a.update(kw)
         return B.attn_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
                                a["D"], a["causal"], a["scale"], a["dtype"], a["ws"], a["wsb"], None)
@@ -123,10 +156,10 @@ def test_host_forward_argument_errors(lib):
     assert call(N=0, q=None, k=None, v=None, o=None, lse=None, ws=None) == B.ATTN_OK
 
 
-def test_backward_argument_errors(lib):
+def test_backward_argument_errors(lib, P):
     def call(**kw):
         a = dict(q=P, k=P, v=P, o=P, lse=P, do=P, dq=P, dk=P, dv=P, B=1, H=2, Nq=16, Nk=40, D=64,
-                 cq=None, ck=None, causal=1, scale=0.125, dtype=B.ATTN_BF16, ws=P, wsb=1 << 30)
+                 cq=None, ck=None, causal=1, scale=0.125, dtype=B.ATTN_BF16, ws=P, wsb=BUF_BYTES)
         a.update(kw)
         return B.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"],
                           a["dv"], a["B"], a["H"], a["Nq"], a["Nk"], a["D"], a["cq"], a["ck"],
@@ -152,7 +185,7 @@ def test_backward_argument_errors(lib):
                 dk=None, dv=None, ws=None) == B.ATTN_OK
 
 
-def test_16bit_head_dims(lib):
+def test_16bit_head_dims(lib, P):
     for fn in (B.attn_fwd, B.attn_fwd_f16):
         for d in (32, 96, 256):
             assert fn(P, P, P, P, P, 1, 1, 16, d, None, 1, 0.1, None) == B.ATTN_ERR_HEADDIM
@@ -160,11 +193,20 @@ def test_16bit_head_dims(lib):
 
 def test_timeout_setter(lib):
     assert B.attn_set_wait_timeout_ns(0) == B.ATTN_ERR_SHAPE
+    assert B.attn_set_wait_timeout_ns(999_999) == B.ATTN_ERR_SHAPE   # below one millisecond
+    assert B.attn_set_wait_timeout_ns(1_000_000) == B.ATTN_OK
     assert B.attn_set_wait_timeout_ns(10**9) == B.ATTN_OK
     assert B.attn_wait_selftest(0, None) == B.ATTN_ERR_SHAPE
 
 
-def test_no_device_means_loud_failure(lib):
+def test_fault_injection_switch(lib):
+    assert B.attn_set_fault_injection(2) == B.ATTN_ERR_SHAPE
+    assert B.attn_set_fault_injection(-1) == B.ATTN_ERR_SHAPE
+    assert B.attn_set_fault_injection(1) == B.ATTN_OK
+    assert B.attn_set_fault_injection(0) == B.ATTN_OK
+
+
+def test_no_device_means_loud_failure(lib, P):
     import torch
     if torch.cuda.is_available():
         pytest.skip("a CUDA device is present")
@@ -177,7 +219,7 @@ def test_no_device_means_loud_failure(lib):
                                 None) == B.ATTN_ERR_LAUNCH
 
 
-def test_decode_argument_errors(lib):
+def test_decode_argument_errors(lib, P):
     def call(**kw):
         a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, H=2, Nq=1, Nk=100, D=128, scale=0.1, ws=None,
                  wsb=0)
@@ -197,3 +239,17 @@ def test_decode_argument_errors(lib):
     assert rc == B.ATTN_ERR_SHAPE
     rc, _ = B.attn_decode_workspace_bytes(1, 1, 1, 10, 80)
     assert rc == B.ATTN_ERR_HEADDIM
+    # B * H beyond 2^24 planes (and beyond the int range) is refused, not wrapped
+    rc, _ = B.attn_decode_workspace_bytes(1 << 16, 1 << 16, 1, 10, 128)
+    assert rc == B.ATTN_ERR_SHAPE
+    rc, _ = B.attn_decode_workspace_bytes(1 << 12, (1 << 12) + 1, 1, 10, 128)
+    assert rc == B.ATTN_ERR_SHAPE
+
+
+def test_read_probe_argument_errors(lib, P):
+    assert B.attn_hbm_read_probe(None, 16, P, None) == B.ATTN_ERR_NULL
+    assert B.attn_hbm_read_probe(P, 16, None, None) == B.ATTN_ERR_NULL
+    assert B.attn_hbm_read_probe(P, 0, P, None) == B.ATTN_ERR_SHAPE
+    assert B.attn_hbm_read_probe(P, 24, P, None) == B.ATTN_ERR_SHAPE
+    assert B.attn_hbm_read_probe(P + 8, 16, P, None) == B.ATTN_ERR_ALIGN
+    assert B.attn_hbm_read_probe(P, 16, P + 2, None) == B.ATTN_ERR_ALIGN

@@ -161,14 +161,23 @@ def test_cross_workload_config_keys(name):
     assert cfg["workload"] == name and cfg["Nk"] == W.CROSS_WORKLOADS[name].n_keys
 
 
-def test_sample_blocks_walk_back_from_the_last_row_and_start_over():
-    blocks, done = [], 0
-    for size in (3, 3, 3, 3):
-        b = bench._sample_block(7, done, size)
-        blocks.append(b.tolist())
-        done += len(b)
-    # 7 rows: 4..6, 1..3, then the short block 0..0, then again from the end
-    assert blocks == [[4, 5, 6], [1, 2, 3], [0], [4, 5, 6]]
+def test_oracle_units_cover_every_plane_and_cap_long_ones():
+    w = W.custom("bf16", B=2, H=3, N=40, D=64, seed=3)
+    units = bench._oracle_units(w, W.generate(w))
+    assert len(units) == 6 and all(u[0].shape == (40, 64) for u in units)
+    v = W.custom("bf16", H=2, D=64, varlen=[5, 9000, 3], seed=4)
+    units = bench._oracle_units(v, W.generate(v))
+    # one unit per (sequence, head); the long sequence keeps its last rows, all keys
+    assert [u[0].shape[0] for u in units] == [5, 5, bench.UNIT_ROWS, bench.UNIT_ROWS, 3, 3]
+    assert units[2][1].shape[0] == 9000
+
+
+def test_unit_flops_count_allowed_pairs():
+    q, k = np.zeros((3, 8)), np.zeros((5, 8))
+    # last 3 queries of a 5-key causal plane see 3, 4 and 5 keys
+    assert bench._unit_flops(q, k, True, 8) == 4 * 8 * (3 + 4 + 5)
+    assert bench._unit_flops(q, k, False, 8) == 4 * 8 * 15
+    assert bench._unit_flops(k, k, True, 8) == 4 * 8 * 15
 
 
 def test_host_cores_respects_the_affinity_mask():
@@ -182,7 +191,7 @@ def test_cpu_baseline_on_a_small_workload():
     # the process pool (spawned workers) and the one-process figure
     w = W.WORKLOADS["f32_causal_b2_h4_n128_d64"]
     x = W.generate(w)
-    r = bench.cpu_baseline(w, x, budget_s=0.5)
+    r = bench.cpu_baseline(w, x, cpu_seconds=0.5)
     assert r["kind"] == "oracle" and r["value"] > 0 and r["value_1core"] > 0
     assert 1 <= r["cores"] <= bench.host_cores()
-    assert "query rows of plane (b=0,h=0)" in r["sample"]
+    assert "oracle.attention_plane" in r["sample"] and "whole planes" in r["sample"]

@@ -122,3 +122,21 @@ def test_library_allocates_no_device_memory():
     free1, _ = torch.cuda.mem_get_info()
     assert torch.cuda.max_memory_allocated() == peak0
     assert abs(free1 - free0) < (2 << 20)
+
+
+@pytest.mark.parametrize("nbytes", [16, 16 * 12345, 64 << 20])
+def test_hbm_read_probe_reads_every_word(nbytes):
+    # the probe folds every 32-bit word it reads with XOR: the fold must equal
+    # the host's, so the bandwidth it times is the bandwidth of reading it all
+    import torch
+    from exact_io_aware_107_b300 import _binding
+    rng = np.random.default_rng(nbytes % 1000)
+    host = rng.integers(0, 2**32, nbytes // 4, dtype=np.uint32)
+    buf = torch.from_numpy(host.view(np.int32)).cuda()
+    out = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream()
+    assert _binding.attn_hbm_read_probe(buf.data_ptr(), nbytes, out.data_ptr(), s.cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert int(out.cpu().numpy().view(np.uint32)[0]) == int(np.bitwise_xor.reduce(host))
+    assert _binding.attn_hbm_read_probe(buf.data_ptr(), 8, out.data_ptr(), s.cuda_stream) == \
+        _binding.ATTN_ERR_SHAPE
