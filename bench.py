@@ -247,13 +247,9 @@ def host_cores() -> int:
 
 
 def _blas_single_thread():
-    """One BLAS thread per worker thread, when threadpoolctl is available."""
-    try:
-        from threadpoolctl import threadpool_limits
-        return threadpool_limits(limits=1)
-    except ImportError:
-        import contextlib
-        return contextlib.nullcontext()
+    """One BLAS thread in this process inside the block (the oracle's helper)."""
+    from oracle.threads import blas_threads
+    return blas_threads(1)
 
 
 # The oracle is timed in the form the parity tests run it: oracle.attention_plane
@@ -311,11 +307,8 @@ def _oracle_unit(job):
 
 
 def _oracle_worker_init():
-    try:
-        from threadpoolctl import threadpool_limits
-        threadpool_limits(limits=1)
-    except ImportError:
-        pass
+    from oracle.threads import set_blas_threads
+    set_blas_threads(1)
 
 
 class OraclePool:
@@ -329,16 +322,21 @@ class OraclePool:
         if procs > 1:
             import multiprocessing as mp
             from concurrent.futures import ProcessPoolExecutor
-            self.ex = ProcessPoolExecutor(max_workers=procs, mp_context=mp.get_context("spawn"),
-                                          initializer=_oracle_worker_init)
-            # start every worker (and its imports) before anything is timed
-            tiny = (np.zeros((4, w.D), np.float32),) * 3
-            try:
-                list(self.ex.map(_oracle_unit, [tiny + (w.scale, w.causal)] * (2 * procs),
-                                 timeout=300))
-            except Exception:  # noqa: BLE001 - any failure: measure in-process instead
-                self.ex.shutdown(wait=False, cancel_futures=True)
-                self.ex, self.procs = None, 1
+            from oracle.threads import single_thread_children
+            # the workers read OPENBLAS_NUM_THREADS=1 (and its OpenMP/MKL
+            # equivalents) when their BLAS loads; the initialiser sets it again
+            with single_thread_children():
+                self.ex = ProcessPoolExecutor(max_workers=procs,
+                                              mp_context=mp.get_context("spawn"),
+                                              initializer=_oracle_worker_init)
+                # start every worker (and its imports) before anything is timed
+                tiny = (np.zeros((4, w.D), np.float32),) * 3
+                try:
+                    list(self.ex.map(_oracle_unit, [tiny + (w.scale, w.causal)] * (2 * procs),
+                                     timeout=300))
+                except Exception:  # noqa: BLE001 - any failure: measure in-process instead
+                    self.ex.shutdown(wait=False, cancel_futures=True)
+                    self.ex, self.procs = None, 1
 
     def round(self):
         """One round: the next `procs` units (cycling over the workload), one per

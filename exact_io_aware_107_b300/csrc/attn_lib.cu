@@ -268,12 +268,16 @@ int fwd_16bit(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.rows = Nq;
   p.rows_k = Nk;
   p.n_qblk = (Nq + 255) / 256;
-  // work items: packed -> single 256-row blocks (an upper bound, surplus
-  // entries are skipped); dense -> pairs of mirror blocks of one plane
-  const long long tiles = cu_q ? (1LL * (Nq / 256 + B) * H) : (1LL * p.n_qblk * planes);
-  const long long items = cu_q ? tiles : 1LL * ((p.n_qblk + 1) / 2) * planes;
-  if (tiles > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-  p.n_tiles = static_cast<int>(tiles);
+  // work items: packed -> pairs of mirror blocks of one sequence and head (an
+  // upper bound: the sequences' blocks number at most Nq/256 + B, so their
+  // pairs at most half that plus B); dense causal -> pairs of mirror blocks of
+  // one plane; dense non-causal -> single blocks, the last round possibly
+  // split into single query tiles (up to twice as many CTAs as blocks)
+  const long long blocks = 1LL * p.n_qblk * planes;
+  const long long items = cu_q ? 1LL * ((Nq / 256 + B) / 2 + B) * H
+                               : (causal ? 1LL * ((p.n_qblk + 1) / 2) * planes : 2 * blocks);
+  if (items > 0x7fffffffLL || blocks > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  p.n_tiles = static_cast<int>(items);
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.stall = g_stall.load();

@@ -67,13 +67,16 @@ struct Bf16Params {
   int rows;                 // query rows per plane (dense: Nq; packed: total query tokens)
   int rows_k;               // key rows per plane (dense: Nk; packed: total key tokens)
   int n_qblk;               // dense: ceil(Nq/256)
-  int n_tiles;            // packed: an upper bound on the work tiles
+  int n_tiles;            // packed: an upper bound on the work items (block pairs)
   int causal;
   float scale_log2;       // scale * log2(e)
   int stall;              // abort-path test: CTA 0 waits on a phase nothing completes
   unsigned long long timeout_ns;
   unsigned int* err;
 };
+
+// Packed layouts with at most this many sequences take them longest first.
+constexpr int kSortMaxSeq = 256;
 
 template <int D>
 struct Bf16Cfg {
@@ -90,7 +93,9 @@ struct Bf16Cfg {
   // o_full[2], mma_done
   static constexpr int NBAR = 4 + 2 * NSTAGE + 6 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-  static constexpr int SMEM_BYTES = MISC_OFF + 16;
+  // packed layout: the sequences in decreasing length (up to kSortMaxSeq of them)
+  static constexpr int ORDER_OFF = MISC_OFF + 16;
+  static constexpr int SMEM_BYTES = ORDER_OFF + 2 * kSortMaxSeq;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
   static constexpr int THREADS = 320;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -100,93 +105,148 @@ struct Bf16Cfg {
   static_assert(SMEM_ALLOC <= 232448, "shared memory");
 };
 
-// One work tile: 256 query rows of one plane / sequence.
+// One work tile: up to 256 query rows (two 128-row query tiles) of one plane
+// or sequence.
 struct WorkTile {
   int plane;     // tensor-map plane coordinate (dense: b*H+h; packed: h)
   int row_base;  // first query row of the sequence in the query map (0 when dense)
   int seq_len;   // query rows of the sequence
   int kv_base;   // first key row of the sequence in the key/value maps
   int kv_len;    // keys of the sequence
-  int qblk;      // 256-row block index within the sequence
-  bool has_q1;   // the block has a second 128-row query tile
+  int q0;        // first row of query tile 0 within the sequence (tile 1 follows it)
+  bool has_q1;   // a second 128-row query tile follows
   int n0, n1;    // key tiles visited by query tile 0 and 1 (0: none, or tile absent)
 };
 
-// Cursor over packed sequences; every CTA's list positions increase, so the
-// walk over cu_seqlens only moves forward.
+// Cursor over packed sequences (in the order the schedule takes them); every
+// CTA's list positions increase, so the walk over cu_seqlens only moves forward.
 struct SeqCursor {
   int s = 0;
-  int cum = 0;  // 256-row blocks of the sequences before s
+  int cum = 0;  // work items of the sequences before position s
 };
+
+// The packed sequences in decreasing length (ties by index) into order[]:
+// each thread ranks some of them against all.  The comparison is a strict
+// total order, so the ranks are a permutation whatever cu_seqlens holds (a
+// malformed array is caught later, when the walk reads the entry).
+__device__ __forceinline__ void bf16_sort_sequences(const Bf16Params& p, uint16_t* order) {
+  for (int s = threadIdx.x; s < p.nseq; s += blockDim.x) {
+    const int len = __ldg(p.cu_seqlens + s + 1) - __ldg(p.cu_seqlens + s);
+    int rank = 0;
+    for (int t = 0; t < p.nseq; ++t) {
+      const int lt = __ldg(p.cu_seqlens + t + 1) - __ldg(p.cu_seqlens + t);
+      rank += (lt > len) || (lt == len && t < s);
+    }
+    order[rank] = static_cast<uint16_t>(s);
+  }
+}
 
 enum TileStep { kTileEnd = 0, kTileRun = 1, kTileSkip = 2 };
 
 // The it-th work tile of this CTA.
 //
-// Dense layout: the work list holds pairs of 256-row blocks of one plane,
-// block b with its mirror n-1-b, so that every pair costs the same under the
-// causal mask; pairs are plane-major (the CTAs in flight share few planes and
-// their K/V stay in L2).  Rounds of gridDim.x pairs go to the CTAs in
-// alternating direction; a CTA runs the heavy block of its pair, then the
+// Dense causal layout: the work list holds pairs of 256-row blocks of one
+// plane, block b with its mirror n-1-b, so that every pair costs the same
+// under the causal mask; pairs are plane-major (the CTAs in flight share few
+// planes and their K/V stay in L2).  Rounds of gridDim.x pairs go to the CTAs
+// in alternating direction; a CTA runs the heavy block of its pair, then the
 // light one (iteration it: pair round it/2, half it%2).
 //
-// Packed layout: the list holds single blocks, sequence by sequence, heaviest
-// block first, heads innermost; rounds alternate direction the same way.
+// Dense non-causal layout: every block costs the same, so the list holds
+// single blocks, plane-major, one round of gridDim.x per iteration.  When the
+// last round is at most half full, its blocks are split into single 128-row
+// query tiles, one per CTA, so that the last round takes about half as long.
+//
+// Packed layout: pairs of mirror blocks within one sequence of one head, the
+// pairs of a (sequence, head) consecutive (its K/V stays in L2), the heads of
+// a sequence next, and the sequences longest first (order[], when the kernel
+// could sort them; else as given), so that the pairs, whose cost grows with
+// the sequence length, come in decreasing cost; rounds alternate direction as
+// for dense pairs.
 //
 // Returns kTileEnd past the last tile (or when cu_seqlens is malformed),
 // kTileSkip for the empty second half of a pair whose two blocks coincide.
 // A query tile whose rows see no key at all has n_i == 0: no loads and no
 // MMAs, its softmax warps write O = 0 and LSE = -inf directly.
-__device__ __forceinline__ int bf16_tile(const Bf16Params& p, int it, SeqCursor& cur,
-                                         WorkTile& w) {
+__device__ __forceinline__ int bf16_tile(const Bf16Params& p, const uint16_t* order, int it,
+                                         SeqCursor& cur, WorkTile& w) {
   const int grid = static_cast<int>(gridDim.x);
   const int c = static_cast<int>(blockIdx.x);
+  bool single = false;  // one 128-row query tile only
   if (p.cu_seqlens == nullptr) {
-    const int round = it >> 1;
-    const int pair = round * grid + ((round & 1) ? grid - 1 - c : c);
-    const int npp = (p.n_qblk + 1) / 2;  // pairs per plane
-    if (pair >= p.planes * npp) return kTileEnd;
-    w.plane = pair / npp;
-    const int pb = pair - w.plane * npp;
-    const int heavy = p.n_qblk - 1 - pb;
-    if (it & 1) {
-      if (pb == heavy) return kTileSkip;
-      w.qblk = pb;
-    } else {
-      w.qblk = heavy;
-    }
     w.row_base = 0;
     w.seq_len = p.rows;
     w.kv_base = 0;
     w.kv_len = p.rows_k;
+    if (p.causal) {
+      const int round = it >> 1;
+      const int pair = round * grid + ((round & 1) ? grid - 1 - c : c);
+      const int npp = (p.n_qblk + 1) / 2;  // pairs per plane
+      if (pair >= p.planes * npp) return kTileEnd;
+      w.plane = pair / npp;
+      const int pb = pair - w.plane * npp;
+      const int heavy = p.n_qblk - 1 - pb;
+      if (it & 1) {
+        if (pb == heavy) return kTileSkip;
+        w.q0 = pb * 256;
+      } else {
+        w.q0 = heavy * 256;
+      }
+    } else {
+      const int nblk = p.planes * p.n_qblk;
+      const int full = nblk / grid;  // rounds with a block for every CTA
+      const int rem = nblk - full * grid;
+      int u;
+      if (it < full) {
+        u = it * grid + c;
+      } else {
+        if (it > full || rem == 0) return kTileEnd;
+        single = 2 * rem <= grid;
+        if (c >= (single ? 2 * rem : rem)) return kTileEnd;
+        u = full * grid + (single ? c / 2 : c);
+      }
+      w.plane = u / p.n_qblk;
+      w.q0 = (u - w.plane * p.n_qblk) * 256 + (single ? 128 * (c & 1) : 0);
+      if (w.q0 >= w.seq_len) return kTileEnd;  // the second tile of a short last block
+    }
   } else {
-    const int u = it * grid + ((it & 1) ? grid - 1 - c : c);
+    const int round = it >> 1;
+    const int u = round * grid + ((round & 1) ? grid - 1 - c : c);
     if (u >= p.n_tiles) return kTileEnd;
-    const int vb = u / p.planes;
-    w.plane = u - vb * p.planes;
     bool found = false;
     while (cur.s < p.nseq) {
-      const int a = __ldg(p.cu_seqlens + cur.s), e = __ldg(p.cu_seqlens + cur.s + 1);
+      const int sq = order ? static_cast<int>(order[cur.s]) : cur.s;
+      const int a = __ldg(p.cu_seqlens + sq), e = __ldg(p.cu_seqlens + sq + 1);
       if (a < 0 || e < a || e > p.rows) {
         if (threadIdx.x == 0) atomicOr(p.err, kDevErrBounds);
         return kTileEnd;
       }
       const int nb = (e - a + 255) / 256;
-      if (vb < cur.cum + nb) {
-        const int ak = __ldg(p.cu_seqlens_k + cur.s), ek = __ldg(p.cu_seqlens_k + cur.s + 1);
+      const int npp = (nb + 1) / 2;
+      if (u < cur.cum + npp * p.planes) {
+        const int ak = __ldg(p.cu_seqlens_k + sq), ek = __ldg(p.cu_seqlens_k + sq + 1);
         if (ak < 0 || ek < ak || ek > p.rows_k) {
           if (threadIdx.x == 0) atomicOr(p.err, kDevErrBounds);
           return kTileEnd;
+        }
+        const int r = u - cur.cum;
+        w.plane = r / npp;
+        const int pb = r - w.plane * npp;
+        const int heavy = nb - 1 - pb;
+        if (it & 1) {
+          if (pb == heavy) return kTileSkip;
+          w.q0 = pb * 256;
+        } else {
+          w.q0 = heavy * 256;
         }
         w.row_base = a;
         w.seq_len = e - a;
         w.kv_base = ak;
         w.kv_len = ek - ak;
-        w.qblk = nb - 1 - (vb - cur.cum);
         found = true;
         break;
       }
-      cur.cum += nb;
+      cur.cum += npp * p.planes;
       ++cur.s;
     }
     if (!found) return kTileEnd;
@@ -199,9 +259,9 @@ __device__ __forceinline__ int bf16_tile(const Bf16Params& p, int it, SeqCursor&
     const int last = min(q0 + 127, w.seq_len - 1) + off;
     return last < 0 ? 0 : min(nkv, last / 128 + 1);
   };
-  w.has_q1 = w.qblk * 256 + 128 < w.seq_len;
-  w.n0 = visited(w.qblk * 256);
-  w.n1 = w.has_q1 ? visited(w.qblk * 256 + 128) : 0;
+  w.has_q1 = !single && w.q0 + 128 < w.seq_len;
+  w.n0 = visited(w.q0);
+  w.n1 = w.has_q1 ? visited(w.q0 + 128) : 0;
   return kTileRun;
 }
 
@@ -256,10 +316,17 @@ __global__ void __launch_bounds__(320, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
+  // packed layout: every role walks the sequences in the same order
+  uint16_t* order = nullptr;
+  if (p.cu_seqlens != nullptr && p.nseq <= kSortMaxSeq) {
+    order = reinterpret_cast<uint16_t*>(smem + C::ORDER_OFF);
+    bf16_sort_sequences(p, order);
+    __syncthreads();
+  }
   {
     SeqCursor c0;
     WorkTile w0;
-    if (bf16_tile(p, 0, c0, w0) != kTileRun) return;  // uniform: no work for this CTA
+    if (bf16_tile(p, order, 0, c0, w0) != kTileRun) return;  // uniform: no work for this CTA
   }
 
   const int warp = threadIdx.x / 32;
@@ -305,11 +372,11 @@ __global__ void __launch_bounds__(320, 1)
     SeqCursor cur;
     WorkTile w;
     for (int it = 0;; ++it) {
-      const int step = bf16_tile(p, it, cur, w);
+      const int step = bf16_tile(p, order, it, cur, w);
       if (step == kTileEnd) break;
       if (step == kTileSkip || (ti == 1 && !w.has_q1)) continue;
       const int n_i = ti ? w.n1 : w.n0;
-      const int q_first = w.qblk * 256 + 128 * ti;  // first row of this query tile
+      const int q_first = w.q0 + 128 * ti;  // first row of this query tile
       const int row = q_first + t;
       const int off = w.kv_len - w.seq_len;         // causal alignment of queries to keys
       if (n_i == 0) {
@@ -463,7 +530,7 @@ __global__ void __launch_bounds__(320, 1)
     // commit, so this wait runs out of budget and the whole CTA aborts
     if (p.stall && blockIdx.x == 0) ok = wait(mma_done, 0);
     for (int it = 0; ok; ++it) {
-      const int step = bf16_tile(p, it, cur, w);
+      const int step = bf16_tile(p, order, it, cur, w);
       if (step == kTileEnd) break;
       if (step == kTileSkip) continue;
       const int nmax = max(w.n0, w.n1);
@@ -558,7 +625,7 @@ __global__ void __launch_bounds__(320, 1)
       return true;
     };
     for (int it = 0; ok; ++it) {
-      const int step = bf16_tile(p, it, cur, w);
+      const int step = bf16_tile(p, order, it, cur, w);
       if (step == kTileEnd) break;
       if (step == kTileSkip) continue;
       const int nkv = 2 * max(w.n0, w.n1);
@@ -575,7 +642,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d_warp(smem_base + C::Q_OFF + ti * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ,
-                           smem_u32(&q_full[ti]), c * 64, w.row_base + w.qblk * 256 + 128 * ti,
+                           smem_u32(&q_full[ti]), c * 64, w.row_base + w.q0 + 128 * ti,
                            w.plane);
         ++n_q[ti];
       }

@@ -74,6 +74,17 @@ def test_bf16_varlen_small(causal, D):
     _full_compare(w, BF16_TOL_O, BF16_TOL_LSE)
 
 
+@pytest.mark.parametrize("nseq", [256, 300])
+def test_bf16_varlen_many_sequences(nseq):
+    # up to 256 sequences are taken longest first (sorted inside the kernel);
+    # more are taken in the order given: both orders against the oracle
+    rng = np.random.default_rng(nseq)
+    lens = rng.integers(0, 700, nseq).tolist()
+    lens[::37] = [0] * len(lens[::37])                  # some empty sequences
+    w = W.custom("bf16", H=2, D=64, causal=True, seed=nseq, varlen=lens)
+    _full_compare(w, BF16_TOL_O, BF16_TOL_LSE)
+
+
 def test_bf16_peaked_small():
     # Q, K ~ N(0, 2^2): scores with std 4, rows near one-hot, many reference-max moves
     w = W.custom("bf16", B=1, H=4, N=1500, D=128, causal=True, seed=3, qk_std=2.0)
@@ -184,7 +195,7 @@ def _oracle_threads():
 def test_workload_every_element(name):
     import time
     from concurrent.futures import ThreadPoolExecutor
-    from threadpoolctl import threadpool_limits
+    from oracle.threads import blas_threads
     w = W.WORKLOADS[name]
     x = W.generate(w)
     o, lse = run_cuda(x["q"], x["k"], x["v"], w.causal, w.scale, x["cu_seqlens"])
@@ -210,7 +221,7 @@ def test_workload_every_element(name):
         return max_err(o[idx], ro), max_err(lse[idx], rl)
 
     t0 = time.perf_counter()
-    with threadpool_limits(limits=1):
+    with blas_threads(1):
         with ThreadPoolExecutor(max_workers=_oracle_threads()) as ex:
             errs = list(ex.map(one, jobs))
     secs = time.perf_counter() - t0
@@ -249,7 +260,7 @@ def test_many_planes_several_blocks_every_element(N, causal):
     # 160 planes of 5 blocks of 256 rows: 480 mirror pairs over the persistent
     # CTAs, several rounds in alternating direction, every plane compared in full
     from concurrent.futures import ThreadPoolExecutor
-    from threadpoolctl import threadpool_limits
+    from oracle.threads import blas_threads
     B, H, D = 4, 40, 128
     w = W.custom("bf16", B=B, H=H, N=N, D=D, causal=causal, seed=N + causal)
     x = W.generate(w)
@@ -261,7 +272,7 @@ def test_many_planes_several_blocks_every_element(N, causal):
         ro, rl = oracle.attention_plane(q[b, h], k[b, h], v[b, h], w.scale, causal)
         return max_err(o[b, h], ro), max_err(lse[b, h], rl)
 
-    with threadpool_limits(limits=1):
+    with blas_threads(1):
         with ThreadPoolExecutor(max_workers=_oracle_threads()) as ex:
             errs = list(ex.map(one, [(b, h) for b in range(B) for h in range(H)]))
     eo, el = max(e[0] for e in errs), max(e[1] for e in errs)
