@@ -66,6 +66,90 @@ void launch_decode_kernel(unsigned grid, cudaStream_t s, const CUtensorMap& mk,
   attn_decode_bf16_kernel<D><<<grid, DecCfg<D>::THREADS, DecCfg<D>::SMEM_ALLOC, s>>>(mk, mv, p);
 }
 
+// Read-only stream of device memory (a measurement helper): one CTA per SM
+// copies chunks of 32 KB with 1-D TMA bulk copies into a 4-stage shared-memory
+// ring (128 KB in flight per SM, the form that reads HBM fastest on B300) and
+// folds every 32-bit word with XOR; each warp XORs its fold into *out, so the
+// data is really read.  Every wait is bounded; after an abort the CTA still
+// waits for the copies it issued before it exits.
+constexpr int kProbeStages = 4;
+constexpr int kProbeChunk = 32768;
+constexpr int kProbeSmem = kProbeStages * kProbeChunk + 64;
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(256)
+    hbm_read_probe_kernel(const uint8_t* __restrict__ p, unsigned long long bytes,
+                          unsigned int* out, unsigned long long timeout, unsigned int* err) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* ring = smem_raw;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + kProbeStages * kProbeChunk);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + kProbeStages);
+  const unsigned long long nchunks = (bytes + kProbeChunk - 1) / kProbeChunk;
+  const unsigned long long mine =
+      nchunks > blockIdx.x ? (nchunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kProbeStages; ++s) mbar_init(&full[s], 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const WaitCtl ctl{abort_flag, err, timeout};
+  const uint32_t ring_s = smem_u32(ring);
+  auto chunk_bytes = [&](unsigned long long k) {
+    const unsigned long long off = (blockIdx.x + k * gridDim.x) * kProbeChunk;
+    return static_cast<uint32_t>(bytes - off < kProbeChunk ? bytes - off : kProbeChunk);
+  };
+  auto issue = [&](unsigned long long k) {
+    const int s = static_cast<int>(k % kProbeStages);
+    const uint32_t n = chunk_bytes(k);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(&full[s])),
+                 "r"(n)
+                 : "memory");
+    bulk_load(ring_s + s * kProbeChunk, p + (blockIdx.x + k * gridDim.x) * kProbeChunk, n,
+              smem_u32(&full[s]));
+  };
+  if (threadIdx.x == 0)
+    for (unsigned long long k = 0; k < mine && k < kProbeStages; ++k) issue(k);
+  uint32_t acc = 0;
+  unsigned long long k = 0;
+  bool ok = true;
+  for (; k < mine; ++k) {
+    const int s = static_cast<int>(k % kProbeStages);
+    ok = __syncthreads_and(mbar_wait(&full[s], static_cast<uint32_t>((k / kProbeStages) & 1), ctl));
+    if (!ok) break;
+    const uint4* c = reinterpret_cast<const uint4*>(ring + s * kProbeChunk);
+    const int n16 = static_cast<int>(chunk_bytes(k) / 16);
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) {
+      const uint4 a = c[i];
+      acc ^= a.x ^ a.y ^ a.z ^ a.w;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && k + kProbeStages < mine) {
+      fence_proxy_async_smem();  // the generic reads of the slot come before the copy into it
+      issue(k + kProbeStages);
+    }
+  }
+  if (!ok) {
+    if (threadIdx.x == 0)
+      for (unsigned long long d = k; d < mine && d < k + kProbeStages; ++d)
+        mbar_wait_drain(&full[d % kProbeStages],
+                        static_cast<uint32_t>((d / kProbeStages) & 1), ctl);
+    __syncthreads();
+    return;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) atomicXor(out, acc);
+}
+
 // Checks the current device once and fetches what the launches need.
 int prepare_device(DeviceState** out) {
   int dev = 0;
@@ -146,6 +230,11 @@ int prepare_device(DeviceState** out) {
       cudaGetLastError();
       return ATTN_ERR_LAUNCH;
     }
+    if (cudaFuncSetAttribute(hbm_read_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kProbeSmem) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_LAUNCH;
+    }
     const int f32_smem = (2 * kF32BM * 128 + kF32BN * 129) * 4;
     if (cudaFuncSetAttribute(attn_fwd_f32_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              f32_smem) != cudaSuccess) {
@@ -211,30 +300,6 @@ __global__ void wait_selftest_kernel(unsigned long long budget, unsigned int* er
 }
 
 
-
-// Read-only stream of device memory (a measurement helper): every thread reads
-// 16-byte words that skip L1, four loads in flight, and folds them with XOR;
-// each warp folds its lanes and XORs one word into *out, so no load is dead.
-__global__ void __launch_bounds__(512)
-    hbm_read_probe_kernel(const uint4* __restrict__ p, unsigned long long n16,
-                          unsigned int* out) {
-  const unsigned long long stride = static_cast<unsigned long long>(gridDim.x) * blockDim.x;
-  unsigned long long i = static_cast<unsigned long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  uint32_t acc = 0;
-  for (; i + 3 * stride < n16; i += 4 * stride) {
-    const uint4 a = __ldg(p + i), b = __ldg(p + i + stride), c = __ldg(p + i + 2 * stride),
-                d = __ldg(p + i + 3 * stride);
-    acc ^= a.x ^ a.y ^ a.z ^ a.w ^ b.x ^ b.y ^ b.z ^ b.w ^ c.x ^ c.y ^ c.z ^ c.w ^ d.x ^ d.y ^
-           d.z ^ d.w;
-  }
-  for (; i < n16; i += stride) {
-    const uint4 a = __ldg(p + i);
-    acc ^= a.x ^ a.y ^ a.z ^ a.w;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, o);
-  if ((threadIdx.x & 31) == 0) atomicXor(out, acc);
-}
 
 // 16-bit (bf16 or fp16) forward on the tcgen05 kernel.
 int fwd_16bit(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -919,8 +984,8 @@ extern "C" int attn_hbm_read_probe(const void* buf, unsigned long long bytes, un
   DeviceState* st = nullptr;
   const int rc = prepare_device(&st);
   if (rc != ATTN_OK) return rc;
-  hbm_read_probe_kernel<<<4 * st->sms, 512, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(buf), bytes / 16, out);
+  hbm_read_probe_kernel<<<st->sms, 256, kProbeSmem, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint8_t*>(buf), bytes, out, g_timeout_ns.load(), st->err);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 

@@ -306,8 +306,10 @@ int attn_wait_selftest(unsigned long long timeout_ns, void* stream);
 /*
  * Measurement helper, not an attention operation (the pages have no
  * counterpart): reads `bytes` of device memory at `buf` once, as a
- * read-only stream (16-byte loads that skip L1, 4 x SM-count blocks of 512
- * threads), and XORs a fold of the data into the device word *out.  Timed
+ * read-only stream (one block per SM copying 32 KB chunks into a 4-stage
+ * shared-memory ring with 1-D TMA bulk copies), and XORs a fold of every
+ * 32-bit word into the device word *out.  A bounded wait that runs out sets
+ * ATTN_ERR_TIMEOUT in the device error word, as for the other kernels.  Timed
  * with CUDA events around it on `stream`, bytes / time is the read bandwidth
  * that bounds kernels which only read HBM (the KV-cache decode); a copy moves
  * twice the bytes and reaches a lower figure.  buf 16-byte aligned, bytes a
