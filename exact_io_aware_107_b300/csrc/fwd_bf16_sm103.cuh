@@ -34,9 +34,15 @@
 // list, so they agree on the loop bounds without talking to each other.
 //
 // TMEM (512 columns x 128 lanes, fp32 cells):
-//   [  0,128) S0 = Q0 K^T   (P0 as packed bf16 overwrites its first 64 columns)
+//   [  0,128) S0 = Q0 K^T   (D = 128: P0 as packed bf16 overwrites its first 64 columns)
 //   [128,256) S1 = Q1 K^T   (P1 likewise)
 //   [256,256+D) O0, [256+D, 256+2D) O1
+//   D = 64 only: [384,448) P0, [448,512) P1.  With P in its own columns the MMA
+//   warp issues S_i of the next key tile before P_i V of this one, so the
+//   softmax waits only for the S MMAs; it then waits for that P V (p_free)
+//   before it overwrites P_i or rescales O_i.  At D = 128 S_i of the next key
+//   tile must follow P_i V, whose P it overwrites, and the commit after it
+//   also covers that P V, so O_i is quiescent whenever S_i is ready.
 //
 // Shared memory (1024-byte aligned; every tile is 128 rows x D bf16 stored as
 // D/64 chunks of 128 rows x 128 bytes, 128-byte swizzled, as TMA writes them):
@@ -90,8 +96,8 @@ struct Bf16Cfg {
   static constexpr int KV_OFF = 2 * TILE_BYTES;
   static constexpr int BAR_OFF = KV_OFF + NSTAGE * TILE_BYTES;
   // q_full[2], q_empty[2], kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], p_full[2],
-  // o_full[2], mma_done
-  static constexpr int NBAR = 4 + 2 * NSTAGE + 6 + 1;
+  // o_full[2], mma_done, p_free[2]
+  static constexpr int NBAR = 4 + 2 * NSTAGE + 6 + 1 + 2;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   // packed layout: the sequences in decreasing length (up to kSortMaxSeq of them)
   static constexpr int ORDER_OFF = MISC_OFF + 16;
@@ -101,6 +107,11 @@ struct Bf16Cfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
   static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
+  // D = 64 leaves 128 columns free: P gets its own, so that the next S can be
+  // issued before P V (SPLIT_P); at D = 128 P overwrites the first half of S.
+  static constexpr bool SPLIT_P = (D == 64);
+  static constexpr uint32_t P_COL0 = SPLIT_P ? 384 : S_COL0;
+  static constexpr uint32_t P_COL1 = SPLIT_P ? 448 : S_COL1;
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(SMEM_ALLOC <= 232448, "shared memory");
 };
@@ -313,6 +324,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* p_full = s_full + 2;     // [2]
   uint64_t* o_full = p_full + 2;     // [2]
   uint64_t* mma_done = o_full + 2;
+  uint64_t* p_free = mma_done + 1;   // [2] (SPLIT_P: the P V of the last P is complete)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -339,6 +351,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&o_full[i], 1);
+      mbar_init(&p_free[i], 1);
     }
     for (int s = 0; s < NS; ++s) {
       mbar_init(&kv_full[s], 1);
@@ -366,6 +379,8 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
     const uint32_t tS = tmem + lane_off + (ti ? C::S_COL1 : C::S_COL0);
     const uint32_t tO = tmem + lane_off + (ti ? C::O_COL1 : C::O_COL0);
+    const uint32_t tP = tmem + lane_off + (ti ? C::P_COL1 : C::P_COL0);
+    uint32_t n_pst = 0;  // P tiles stored by this warpgroup so far (SPLIT_P)
     const float cl2 = p.scale_log2;
     const uint64_t c2 = f32x2(cl2, cl2);
     uint32_t n_s = 0, n_o = 0;  // s_full / o_full phases consumed so far
@@ -428,6 +443,18 @@ __global__ void __launch_bounds__(320, 1)
                                  fmaxf(__uint_as_float(sr[126]), __uint_as_float(sr[127])));
         const float mraw = fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], tail);
         const float mt = mraw * cl2;
+        if constexpr (C::SPLIT_P) {
+          // The S just loaded was issued before the P V of the previous key
+          // tile: that P V must be complete before its P columns are
+          // overwritten and O is rescaled (it has had the load's latency to
+          // finish, so this rarely waits).
+          if (n_pst > 0 && !__all_sync(0xffffffffu, mbar_wait(&p_free[ti], (n_pst - 1) & 1, ctl))) {
+            ok = false;
+            break;
+          }
+          ++n_pst;
+          tc_fence_after();
+        }
         float m_new = m_ref;
         float alpha = 1.f;
         bool resc = false;
@@ -461,8 +488,8 @@ __global__ void __launch_bounds__(320, 1)
         const float tile_sum = lo_f32(sum2) + hi_f32(sum2);
         l = l * alpha + tile_sum;
         l_o = l_o * alpha + (tile_sum + pmx_err);
-        tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         if (__any_sync(0xffffffffu, resc)) {
           const float f = resc ? alpha : 1.f;
           const uint64_t f2 = f32x2(f, f);
@@ -575,15 +602,32 @@ __global__ void __launch_bounds__(320, 1)
           tc_fence_after();
           const uint32_t sc = ti ? C::S_COL1 : C::S_COL0;
           const uint32_t oc = ti ? C::O_COL1 : C::O_COL0;
-          bf16_issue_pv<D, F16>(tmem + oc, tmem + sc, vd0 + (gv % NS) * kSlotDesc, j > 0 ? 1u : 0u);
-          // V_j is free for the producer as soon as its last reader is done
-          if (ti == ((j < w.n1) ? 1 : 0)) umma_commit_warp(&kv_empty[gv % NS]);
-          if (j + 1 < n_i) {
-            bf16_issue_s<D, F16>(tmem + sc, qd[ti], kd0 + (gk % NS) * kSlotDesc);
-            umma_commit_warp(&s_full[ti]);
-            if (j + 2 == n_i) umma_commit_warp(&q_empty[ti]);  // that was the last S of Q_ti
+          const uint32_t pc = ti ? C::P_COL1 : C::P_COL0;
+          if constexpr (C::SPLIT_P) {
+            // S of the next key tile first: the softmax waits for it, while
+            // this P V runs behind it
+            if (j + 1 < n_i) {
+              bf16_issue_s<D, F16>(tmem + sc, qd[ti], kd0 + (gk % NS) * kSlotDesc);
+              umma_commit_warp(&s_full[ti]);
+              if (j + 2 == n_i) umma_commit_warp(&q_empty[ti]);  // that was the last S of Q_ti
+            }
+            bf16_issue_pv<D, F16>(tmem + oc, tmem + pc, vd0 + (gv % NS) * kSlotDesc,
+                                  j > 0 ? 1u : 0u);
+            umma_commit_warp(&p_free[ti]);
+            if (ti == ((j < w.n1) ? 1 : 0)) umma_commit_warp(&kv_empty[gv % NS]);
+            if (j + 1 >= n_i) umma_commit_warp(&o_full[ti]);
           } else {
-            umma_commit_warp(&o_full[ti]);
+            bf16_issue_pv<D, F16>(tmem + oc, tmem + pc, vd0 + (gv % NS) * kSlotDesc,
+                                  j > 0 ? 1u : 0u);
+            // V_j is free for the producer as soon as its last reader is done
+            if (ti == ((j < w.n1) ? 1 : 0)) umma_commit_warp(&kv_empty[gv % NS]);
+            if (j + 1 < n_i) {
+              bf16_issue_s<D, F16>(tmem + sc, qd[ti], kd0 + (gk % NS) * kSlotDesc);
+              umma_commit_warp(&s_full[ti]);
+              if (j + 2 == n_i) umma_commit_warp(&q_empty[ti]);  // that was the last S of Q_ti
+            } else {
+              umma_commit_warp(&o_full[ti]);
+            }
           }
         }
         if (!ok) break;
