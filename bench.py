@@ -461,22 +461,26 @@ def workload_config(w):
 # CUDA path
 # ---------------------------------------------------------------------------
 
-def graph_step_ms(step, steps, stream, dev):
+def graph_step_ms(step, steps, stream, dev, reps=1):
     """Milliseconds per step of `steps` calls of step(stream) captured into one
     CUDA graph and replayed (the same kernels back to back, without host
-    launch gaps); None when the capture is refused."""
+    launch gaps); the median over `reps` replays; None when the capture is
+    refused."""
     g = capture_graph(step, steps, stream, dev)
     if g is None:
         return None
     import torch
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        g.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / steps
+    times = []
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / steps)
+    return statistics.median(times)
 
 
 def capture_graph(step, steps, stream, dev):
@@ -551,11 +555,22 @@ def time_steps(call, steps, warmup, stream, dev, local, ws, flush_needed):
         ms, how = starts[0].elapsed_time(ends[0]) / steps, "one CUDA graph of the K steps"
     else:
         ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / steps
+        how = "per-launch CUDA events (graph capture refused)"
         if flush is not None:
-            how = "per-launch CUDA events, L2 flushed (256 MB written) before each launch"
+            # Per-launch events can include host time: the GPU may reach the
+            # start event before the call has been enqueued.  One graph of the
+            # K (flush, call) pairs minus one graph of the K flushes alone gives
+            # the calls' device time after a flush, with no host in between.
+            both = graph_step_ms(lambda st: (flush.zero_(), call(st)), steps, stream, dev,
+                                 reps=3)
+            alone = graph_step_ms(lambda st: flush.zero_(), steps, stream, dev, reps=3)
+            if both is not None and alone is not None and both > alone:
+                ms = both - alone
+                how = ("L2 flushed (256 MB written) before each launch: one CUDA graph of the "
+                       "K (flush, launch) pairs minus one graph of the K flushes")
+            else:
+                how = "per-launch CUDA events, L2 flushed (256 MB written) before each launch"
             warm = graph_step_ms(call, steps, stream, dev)
-        else:
-            how = "per-launch CUDA events (graph capture refused)"
     return ms, how, clk.summary(), warm
 
 
