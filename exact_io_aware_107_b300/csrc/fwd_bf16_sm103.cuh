@@ -428,20 +428,7 @@ __global__ void __launch_bounds__(320, 1)
           for (int c = 0; c < 128; ++c)
             if (kv0 + c > lim) sr[c] = __float_as_uint(-INFINITY);
         }
-        // row max: four independent chains of three-input maxima
-        float mx[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          mx[e] = fmax3(__uint_as_float(sr[e]), __uint_as_float(sr[e + 4]),
-                        __uint_as_float(sr[e + 8]));
-#pragma unroll
-        for (int c = 12; c < 124; c += 8)
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            mx[e] = fmax3(mx[e], __uint_as_float(sr[c + e]), __uint_as_float(sr[c + 4 + e]));
-        const float tail = fmax3(__uint_as_float(sr[124]), __uint_as_float(sr[125]),
-                                 fmaxf(__uint_as_float(sr[126]), __uint_as_float(sr[127])));
-        const float mraw = fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], tail);
+        const float mraw = row_max<128>(sr);
         const float mt = mraw * cl2;
         if constexpr (C::SPLIT_P) {
           // The S just loaded was issued before the P V of the previous key
