@@ -68,7 +68,8 @@ void launch_decode_kernel(unsigned grid, cudaStream_t s, const CUtensorMap& mk,
 
 // Read-only stream of device memory (a measurement helper): one CTA per SM
 // copies chunks of 32 KB with 1-D TMA bulk copies into a 4-stage shared-memory
-// ring (128 KB in flight per SM, the form that reads HBM fastest on B300) and
+// ring (128 KB in flight per SM; TMA bulk rings read HBM fastest in sweeps of
+// load shapes on B300) and
 // folds every 32-bit word with XOR; each warp XORs its fold into *out, so the
 // data is really read.  Every wait is bounded; after an abort the CTA still
 // waits for the copies it issued before it exits.

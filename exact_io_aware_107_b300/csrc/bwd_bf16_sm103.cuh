@@ -139,8 +139,15 @@ struct BwdCfg {
   static constexpr int THREADS = 448;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t DV_COL = 0, DK_COL = D, S_COL = 2 * D, DP_COL = 2 * D + 128;
+  // D = 64 leaves 128 columns free: dQ gets its own, so that dP^T of the next
+  // query tile does not wait for dQ to leave the dP^T columns, and dP^T is one
+  // N = 128 MMA group instead of two halves (DQ_OWN).  At D = 128 dQ reuses the
+  // dP^T columns.
+  static constexpr bool DQ_OWN = (D == 64);
+  static constexpr uint32_t DQ_COL = DQ_OWN ? DP_COL + 128 : DP_COL;
   static_assert(D == 64 || D == 128, "head dim");
-  static_assert(DP_COL + 128 <= TMEM_COLS, "tensor memory");
+  static_assert(DP_COL + 128 <= TMEM_COLS && DQ_COL + (DQ_OWN ? D : 0) <= TMEM_COLS,
+                "tensor memory");
   static_assert(SMEM_ALLOC <= 232448, "shared memory");
 };
 
@@ -448,7 +455,7 @@ __global__ void __launch_bounds__(448, 1)
     // ------------------------------------------------------------ dQ drain
     const int t = threadIdx.x - 256;  // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp - 8)) << 16;
-    const uint32_t tQ = tmem + lane_off + C::DP_COL;
+    const uint32_t tQ = tmem + lane_off + C::DQ_COL;
     // Rows of the tile past the sequence's end carry dQ = 0 exactly (their P
     // and dS columns are zero), so a box that reaches into the next plane's or
     // sequence's rows adds zeros there; rows past the whole tensor are clipped.
@@ -537,16 +544,23 @@ __global__ void __launch_bounds__(448, 1)
         ok = false;
         break;
       }
-      for (int hq = 0; hq < 2; ++hq) {
-        if (i > 0 && !wait(&dq_empty[hq], (i - 1) & 1)) {
-          ok = false;
-          break;
-        }
+      if constexpr (C::DQ_OWN) {
         tc_fence_after();
-        bwd_mma_kk<D>(tDP + 64 * hq, vA, doK + ((hq * 64 * 128) >> 4), id_s64, 0);
-        umma_commit_warp(&dp_full[hq]);
+        bwd_mma_kk<D>(tDP, vA, doK, id_s, 0);
+        umma_commit_warp(&dp_full[0]);
+        umma_commit_warp(&dp_full[1]);
+      } else {
+        for (int hq = 0; hq < 2; ++hq) {
+          if (i > 0 && !wait(&dq_empty[hq], (i - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          bwd_mma_kk<D>(tDP + 64 * hq, vA, doK + ((hq * 64 * 128) >> 4), id_s64, 0);
+          umma_commit_warp(&dp_full[hq]);
+        }
+        if (!ok) break;
       }
-      if (!ok) break;
       // dV += P_i^T dO_i  (P^T from TMEM, 16 queries = 8 packed columns per step)
       if (!wait(p_full, i & 1)) {
         ok = false;
@@ -582,10 +596,18 @@ __global__ void __launch_bounds__(448, 1)
         umma_ts_warp(tDK, tDP + (kk / 4) * 64 + (kk % 4) * 8, qMN[st] + ((kk * 2048) >> 4), id_kv,
                      (i > 0 || kk > 0) ? 1u : 0u);
       umma_commit_warp(&q_empty[st]);
+      if constexpr (C::DQ_OWN) {
+        // the previous dQ must have left its own columns
+        if (i > 0 && (!wait(&dq_empty[0], (i - 1) & 1) || !wait(&dq_empty[1], (i - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        umma_ss_warp(tDP, dsMN + ((kk * 2048) >> 4), kMN + ((kk * 2048) >> 4), id_dq,
-                     kk > 0 ? 1u : 0u);
+        umma_ss_warp(C::DQ_OWN ? tmem + C::DQ_COL : tDP, dsMN + ((kk * 2048) >> 4),
+                     kMN + ((kk * 2048) >> 4), id_dq, kk > 0 ? 1u : 0u);
       umma_commit_warp(dq_full);
       umma_commit_warp(ds_empty);
     }

@@ -37,7 +37,7 @@
 //   [  0,128) S0 = Q0 K^T   (D = 128: P0 as packed bf16 overwrites its first 64 columns)
 //   [128,256) S1 = Q1 K^T   (P1 likewise)
 //   [256,256+D) O0, [256+D, 256+2D) O1
-//   D = 64 only: [384,448) P0, [448,512) P1.  With P in its own columns the MMA
+//   D = 64 (bf16) only: [384,448) P0, [448,512) P1.  With P in its own columns the MMA
 //   warp issues S_i of the next key tile before P_i V of this one, so the
 //   softmax waits only for the S MMAs; it then waits for that P V (p_free)
 //   before it overwrites P_i or rescales O_i.  At D = 128 S_i of the next key
@@ -312,6 +312,12 @@ __global__ void __launch_bounds__(320, 1)
                          const __grid_constant__ CUtensorMap tmV, const Bf16Params p) {
   using C = Bf16Cfg<D>;
   constexpr int NS = C::NSTAGE;
+  // P in its own columns at D = 64 for bf16; the fp16 build of that layout
+  // spills registers at the 168-register cap and runs 6 % slower, so fp16
+  // keeps P in its S columns
+  constexpr bool kSplitP = C::SPLIT_P && !F16;
+  constexpr uint32_t kPCol0 = kSplitP ? C::P_COL0 : C::S_COL0;
+  constexpr uint32_t kPCol1 = kSplitP ? C::P_COL1 : C::S_COL1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -324,7 +330,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* p_full = s_full + 2;     // [2]
   uint64_t* o_full = p_full + 2;     // [2]
   uint64_t* mma_done = o_full + 2;
-  uint64_t* p_free = mma_done + 1;   // [2] (SPLIT_P: the P V of the last P is complete)
+  uint64_t* p_free = mma_done + 1;   // [2] (kSplitP: the P V of the last P is complete)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -379,8 +385,8 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
     const uint32_t tS = tmem + lane_off + (ti ? C::S_COL1 : C::S_COL0);
     const uint32_t tO = tmem + lane_off + (ti ? C::O_COL1 : C::O_COL0);
-    const uint32_t tP = tmem + lane_off + (ti ? C::P_COL1 : C::P_COL0);
-    uint32_t n_pst = 0;  // P tiles stored by this warpgroup so far (SPLIT_P)
+    const uint32_t tP = tmem + lane_off + (ti ? kPCol1 : kPCol0);
+    uint32_t n_pst = 0;  // P tiles stored by this warpgroup so far (kSplitP)
     const float cl2 = p.scale_log2;
     const uint64_t c2 = f32x2(cl2, cl2);
     uint32_t n_s = 0, n_o = 0;  // s_full / o_full phases consumed so far
@@ -430,7 +436,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         const float mraw = row_max<128>(sr);
         const float mt = mraw * cl2;
-        if constexpr (C::SPLIT_P) {
+        if constexpr (kSplitP) {
           // The S just loaded was issued before the P V of the previous key
           // tile: that P V must be complete before its P columns are
           // overwritten and O is rescaled (it has had the load's latency to
@@ -589,8 +595,8 @@ __global__ void __launch_bounds__(320, 1)
           tc_fence_after();
           const uint32_t sc = ti ? C::S_COL1 : C::S_COL0;
           const uint32_t oc = ti ? C::O_COL1 : C::O_COL0;
-          const uint32_t pc = ti ? C::P_COL1 : C::P_COL0;
-          if constexpr (C::SPLIT_P) {
+          const uint32_t pc = ti ? kPCol1 : kPCol0;
+          if constexpr (kSplitP) {
             // S of the next key tile first: the softmax waits for it, while
             // this P V runs behind it
             if (j + 1 < n_i) {
