@@ -23,6 +23,15 @@ namespace attn {
 
 __device__ unsigned int g_dev_error;
 
+// Work counters of the forward kernel's causal and packed schedules: a launch
+// takes the next of kSchedSlots slots (two words each, padded to 32 bytes),
+// which every launch leaves at zero when its last CTA ends.  Launches in
+// flight at the same time use different slots unless kSchedSlots of them are;
+// replays of one captured launch reuse its slot and must not overlap.
+constexpr int kSchedSlots = 256;
+constexpr int kSchedStride = 8;  // words per slot
+__device__ unsigned int g_fwd_sched[kSchedSlots * kSchedStride];
+
 // Scratch of attn_decode_noalloc: the per-slice decode partials of one call
 // (see include/attn_b300.h).  Fixed size, one copy per device, shared by every
 // call of that entry point.
@@ -41,6 +50,8 @@ std::atomic<int> g_stall{0};
 struct DeviceState {
   int checked = 0;  // 0 unknown, 1 ok, -1 wrong arch
   unsigned int* err = nullptr;
+  unsigned int* sched = nullptr;             // g_fwd_sched on this device
+  std::atomic<unsigned int> sched_next{0};   // slot of the next forward launch
   bool attrs_set = false;
   int sms = 0;
 };
@@ -176,6 +187,12 @@ int prepare_device(DeviceState** out) {
         return ATTN_ERR_LAUNCH;
       }
       st.err = static_cast<unsigned int*>(p);
+      void* ps = nullptr;
+      if (cudaGetSymbolAddress(&ps, g_fwd_sched) != cudaSuccess || ps == nullptr) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH;
+      }
+      st.sched = static_cast<unsigned int*>(ps);
       if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
           st.sms < 1) {
         cudaGetLastError();
@@ -337,11 +354,16 @@ int fwd_16bit(const void* q, const void* k, const void* v, void* o, float* lse, 
   // work items: packed -> pairs of mirror blocks of one sequence and head (an
   // upper bound: the sequences' blocks number at most Nq/256 + B, so their
   // pairs at most half that plus B); dense causal -> pairs of mirror blocks of
-  // one plane; dense non-causal -> single blocks, the last round possibly
-  // split into single query tiles (up to twice as many CTAs as blocks)
+  // one plane, then the single blocks of the last tail_planes planes (about
+  // one round of pairs); dense non-causal -> single blocks, the last round
+  // possibly split into single query tiles (up to twice as many CTAs as blocks)
   const long long blocks = 1LL * p.n_qblk * planes;
-  const long long items = cu_q ? 1LL * ((Nq / 256 + B) / 2 + B) * H
-                               : (causal ? 1LL * ((p.n_qblk + 1) / 2) * planes : 2 * blocks);
+  const long long npp = (p.n_qblk + 1) / 2;
+  const long long tail = std::min<long long>(planes, (st->sms + npp - 1) / npp);
+  p.tail_planes = (!cu_q && causal) ? static_cast<int>(tail) : 0;
+  const long long items =
+      cu_q ? 1LL * ((Nq / 256 + B) / 2 + B) * H
+           : (causal ? (planes - tail) * npp + tail * p.n_qblk : 2 * blocks);
   if (items > 0x7fffffffLL || blocks > 0x7fffffffLL) return ATTN_ERR_SHAPE;
   p.n_tiles = static_cast<int>(items);
   p.causal = causal ? 1 : 0;
@@ -349,6 +371,10 @@ int fwd_16bit(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.stall = g_stall.load();
   p.timeout_ns = g_timeout_ns.load();
   p.err = st->err;
+  // the causal and packed schedules hand out their items from a counter
+  p.sched = (cu_q || causal)
+                ? st->sched + (st->sched_next.fetch_add(1) % kSchedSlots) * kSchedStride
+                : nullptr;
 
   const unsigned grid = static_cast<unsigned>(std::min<long long>(items, st->sms));
   if (D == 64) {

@@ -29,9 +29,11 @@
 //   warp  8    tcgen05 MMA issuer (lane 0) and TMEM owner
 //   warp  9    TMA producer (lane 0)
 // A work tile is 256 query rows (two 128-row query tiles) of one (batch,
-// head) plane or of one packed sequence of one head.  Each CTA walks a
-// static list of work tiles (see bf16_tile); every role decodes the same
-// list, so they agree on the loop bounds without talking to each other.
+// head) plane or of one packed sequence of one head.  The TMA producer
+// decodes each tile this CTA runs (the causal and packed layouts take work
+// items from a counter of the launch as they go, the dense non-causal layout
+// walks a static list) and hands it to the MMA and softmax warps through a
+// small ring in shared memory.
 //
 // TMEM (512 columns x 128 lanes, fp32 cells):
 //   [  0,128) S0 = Q0 K^T   (D = 128: P0 as packed bf16 overwrites its first 64 columns)
@@ -74,12 +76,22 @@ struct Bf16Params {
   int rows_k;               // key rows per plane (dense: Nk; packed: total key tokens)
   int n_qblk;               // dense: ceil(Nq/256)
   int n_tiles;            // packed: an upper bound on the work items (block pairs)
+  int tail_planes;        // dense causal: planes handed out as single blocks at the end
   int causal;
   float scale_log2;       // scale * log2(e)
   int stall;              // abort-path test: CTA 0 waits on a phase nothing completes
   unsigned long long timeout_ns;
   unsigned int* err;
+  // Work counter of this launch (next item, CTAs finished), zero at launch
+  // and reset to zero by the last CTA to finish; used by the causal and
+  // packed layouts, whose work items are handed out in order to whichever
+  // CTA asks first.
+  unsigned int* sched;
 };
+
+// Depth of the shared-memory ring through which the TMA producer hands the
+// work tiles it takes to the MMA and softmax warps.
+constexpr int kItemRing = 4;
 
 // Packed layouts with at most this many sequences take them longest first.
 constexpr int kSortMaxSeq = 256;
@@ -96,11 +108,15 @@ struct Bf16Cfg {
   static constexpr int KV_OFF = 2 * TILE_BYTES;
   static constexpr int BAR_OFF = KV_OFF + NSTAGE * TILE_BYTES;
   // q_full[2], q_empty[2], kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], p_full[2],
-  // o_full[2], mma_done, p_free[2]
-  static constexpr int NBAR = 4 + 2 * NSTAGE + 6 + 1 + 2;
+  // o_full[2], mma_done, p_free[2], item_full[kItemRing], item_empty[kItemRing]
+  static constexpr int NBAR = 4 + 2 * NSTAGE + 6 + 1 + 2 + 2 * kItemRing;
+  static constexpr int ITEM_FULL_BAR = 4 + 2 * NSTAGE + 6 + 1 + 2;  // index in the barriers
+  static constexpr int ITEM_EMPTY_BAR = ITEM_FULL_BAR + kItemRing;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  // the work tiles in flight (kItemRing slots of 48 bytes, 16-byte aligned)
+  static constexpr int ITEM_OFF = (MISC_OFF + 16 + 15) / 16 * 16;
   // packed layout: the sequences in decreasing length (up to kSortMaxSeq of them)
-  static constexpr int ORDER_OFF = MISC_OFF + 16;
+  static constexpr int ORDER_OFF = ITEM_OFF + 48 * kItemRing;
   static constexpr int SMEM_BYTES = ORDER_OFF + 2 * kSortMaxSeq;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
   static constexpr int THREADS = 320;
@@ -154,116 +170,12 @@ __device__ __forceinline__ void bf16_sort_sequences(const Bf16Params& p, uint16_
 
 enum TileStep { kTileEnd = 0, kTileRun = 1, kTileSkip = 2 };
 
-// The it-th work tile of this CTA.
-//
-// Dense causal layout: the work list holds pairs of 256-row blocks of one
-// plane, block b with its mirror n-1-b, so that every pair costs the same
-// under the causal mask; pairs are plane-major (the CTAs in flight share few
-// planes and their K/V stay in L2).  Rounds of gridDim.x pairs go to the CTAs
-// in alternating direction; a CTA runs the heavy block of its pair, then the
-// light one (iteration it: pair round it/2, half it%2).
-//
-// Dense non-causal layout: every block costs the same, so the list holds
-// single blocks, plane-major, one round of gridDim.x per iteration.  When the
-// last round is at most half full, its blocks are split into single 128-row
-// query tiles, one per CTA, so that the last round takes about half as long.
-//
-// Packed layout: pairs of mirror blocks within one sequence of one head, the
-// pairs of a (sequence, head) consecutive (its K/V stays in L2), the heads of
-// a sequence next, and the sequences longest first (order[], when the kernel
-// could sort them; else as given), so that the pairs, whose cost grows with
-// the sequence length, come in decreasing cost; rounds alternate direction as
-// for dense pairs.
-//
-// Returns kTileEnd past the last tile (or when cu_seqlens is malformed),
-// kTileSkip for the empty second half of a pair whose two blocks coincide.
-// A query tile whose rows see no key at all has n_i == 0: no loads and no
-// MMAs, its softmax warps write O = 0 and LSE = -inf directly.
-__device__ __forceinline__ int bf16_tile(const Bf16Params& p, const uint16_t* order, int it,
-                                         SeqCursor& cur, WorkTile& w) {
-  const int grid = static_cast<int>(gridDim.x);
-  const int c = static_cast<int>(blockIdx.x);
-  bool single = false;  // one 128-row query tile only
-  if (p.cu_seqlens == nullptr) {
-    w.row_base = 0;
-    w.seq_len = p.rows;
-    w.kv_base = 0;
-    w.kv_len = p.rows_k;
-    if (p.causal) {
-      const int round = it >> 1;
-      const int pair = round * grid + ((round & 1) ? grid - 1 - c : c);
-      const int npp = (p.n_qblk + 1) / 2;  // pairs per plane
-      if (pair >= p.planes * npp) return kTileEnd;
-      w.plane = pair / npp;
-      const int pb = pair - w.plane * npp;
-      const int heavy = p.n_qblk - 1 - pb;
-      if (it & 1) {
-        if (pb == heavy) return kTileSkip;
-        w.q0 = pb * 256;
-      } else {
-        w.q0 = heavy * 256;
-      }
-    } else {
-      const int nblk = p.planes * p.n_qblk;
-      const int full = nblk / grid;  // rounds with a block for every CTA
-      const int rem = nblk - full * grid;
-      int u;
-      if (it < full) {
-        u = it * grid + c;
-      } else {
-        if (it > full || rem == 0) return kTileEnd;
-        single = 2 * rem <= grid;
-        if (c >= (single ? 2 * rem : rem)) return kTileEnd;
-        u = full * grid + (single ? c / 2 : c);
-      }
-      w.plane = u / p.n_qblk;
-      w.q0 = (u - w.plane * p.n_qblk) * 256 + (single ? 128 * (c & 1) : 0);
-      if (w.q0 >= w.seq_len) return kTileEnd;  // the second tile of a short last block
-    }
-  } else {
-    const int round = it >> 1;
-    const int u = round * grid + ((round & 1) ? grid - 1 - c : c);
-    if (u >= p.n_tiles) return kTileEnd;
-    bool found = false;
-    while (cur.s < p.nseq) {
-      const int sq = order ? static_cast<int>(order[cur.s]) : cur.s;
-      const int a = __ldg(p.cu_seqlens + sq), e = __ldg(p.cu_seqlens + sq + 1);
-      if (a < 0 || e < a || e > p.rows) {
-        if (threadIdx.x == 0) atomicOr(p.err, kDevErrBounds);
-        return kTileEnd;
-      }
-      const int nb = (e - a + 255) / 256;
-      const int npp = (nb + 1) / 2;
-      if (u < cur.cum + npp * p.planes) {
-        const int ak = __ldg(p.cu_seqlens_k + sq), ek = __ldg(p.cu_seqlens_k + sq + 1);
-        if (ak < 0 || ek < ak || ek > p.rows_k) {
-          if (threadIdx.x == 0) atomicOr(p.err, kDevErrBounds);
-          return kTileEnd;
-        }
-        const int r = u - cur.cum;
-        w.plane = r / npp;
-        const int pb = r - w.plane * npp;
-        const int heavy = nb - 1 - pb;
-        if (it & 1) {
-          if (pb == heavy) return kTileSkip;
-          w.q0 = pb * 256;
-        } else {
-          w.q0 = heavy * 256;
-        }
-        w.row_base = a;
-        w.seq_len = e - a;
-        w.kv_base = ak;
-        w.kv_len = ek - ak;
-        found = true;
-        break;
-      }
-      cur.cum += npp * p.planes;
-      ++cur.s;
-    }
-    if (!found) return kTileEnd;
-  }
+// The query-tile geometry of w once its plane, rows and q0 are set: the key
+// tiles each of its two query tiles visits (causal: up to the last key its
+// last row may see).  A query tile whose rows see no key at all has n_i == 0:
+// no loads and no MMAs, its softmax warps write O = 0 and LSE = -inf directly.
+__device__ __forceinline__ int bf16_geometry(const Bf16Params& p, WorkTile& w, bool single) {
   const int nkv = (w.kv_len + 127) / 128;
-  // causal: the last key any row of the query tile at q0 may see
   const int off = w.kv_len - w.seq_len;
   auto visited = [&](int q0) {
     if (!p.causal) return nkv;
@@ -274,6 +186,220 @@ __device__ __forceinline__ int bf16_tile(const Bf16Params& p, const uint16_t* or
   w.n0 = visited(w.q0);
   w.n1 = w.has_q1 ? visited(w.q0 + 128) : 0;
   return kTileRun;
+}
+
+// Dense non-causal layout, a static schedule: every 256-row block costs the
+// same, so the list holds single blocks, plane-major, one round of gridDim.x
+// per iteration.  When the last round is at most half full, its blocks are
+// split into single 128-row query tiles, one per CTA, so that the last round
+// takes about half as long.  Returns the it-th tile of this CTA, or kTileEnd.
+__device__ __forceinline__ int bf16_tile_static(const Bf16Params& p, int it, WorkTile& w) {
+  const int grid = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
+  w.row_base = 0;
+  w.seq_len = p.rows;
+  w.kv_base = 0;
+  w.kv_len = p.rows_k;
+  const int nblk = p.planes * p.n_qblk;
+  const int full = nblk / grid;  // rounds with a block for every CTA
+  const int rem = nblk - full * grid;
+  bool single = false;
+  int u;
+  if (it < full) {
+    u = it * grid + c;
+  } else {
+    if (it > full || rem == 0) return kTileEnd;
+    single = 2 * rem <= grid;
+    if (c >= (single ? 2 * rem : rem)) return kTileEnd;
+    u = full * grid + (single ? c / 2 : c);
+  }
+  w.plane = u / p.n_qblk;
+  w.q0 = (u - w.plane * p.n_qblk) * 256 + (single ? 128 * (c & 1) : 0);
+  if (w.q0 >= w.seq_len) return kTileEnd;  // the second tile of a short last block
+  return bf16_geometry(p, w, single);
+}
+
+// Work item u of the causal dense and the packed layouts; half h = 0 is its
+// first (heavier) 256-row block, h = 1 its second, if any.  The items are
+// handed out in list order to whichever CTA asks first, and the list runs
+// from heavy to light, so the CTAs end within about one light item of each
+// other.
+//
+// Dense causal: pairs of 256-row blocks of one plane, block b with its mirror
+// n-1-b, so that every pair costs the same under the causal mask; pairs are
+// plane-major (the CTAs in flight share few planes and their K/V stay in
+// L2).  The last tail_planes planes (about one round of pairs) come as single
+// blocks instead, heaviest first (block n-1 of each of those planes, then
+// block n-2, ...), which fills the last round evenly.
+//
+// Packed: pairs of mirror blocks within one sequence of one head, the pairs
+// of a (sequence, head) consecutive (its K/V stays in L2), the heads of a
+// sequence next, and the sequences longest first (order[], when the kernel
+// could sort them; else as given), so that the pairs, whose cost grows with
+// the sequence length, come in decreasing cost.  A CTA's items come in
+// increasing u, so its walk over cu_seqlens (cur) only moves forward.
+//
+// Returns kTileEnd past the last item (or when cu_seqlens is malformed) and
+// kTileSkip for a half that does not exist.
+__device__ __forceinline__ int bf16_item(const Bf16Params& p, const uint16_t* order, int u, int h,
+                                         SeqCursor& cur, WorkTile& w) {
+  if (p.cu_seqlens == nullptr) {
+    w.row_base = 0;
+    w.seq_len = p.rows;
+    w.kv_base = 0;
+    w.kv_len = p.rows_k;
+    const int npp = (p.n_qblk + 1) / 2;  // pairs per plane
+    const int pair_planes = p.planes - p.tail_planes;
+    const int n_pairs = pair_planes * npp;
+    if (u < n_pairs) {
+      w.plane = u / npp;
+      const int pb = u - w.plane * npp;
+      const int heavy = p.n_qblk - 1 - pb;
+      if (h) {
+        if (pb == heavy) return kTileSkip;
+        w.q0 = pb * 256;
+      } else {
+        w.q0 = heavy * 256;
+      }
+    } else {
+      const int v = u - n_pairs;
+      if (v >= p.tail_planes * p.n_qblk) return kTileEnd;
+      if (h) return kTileSkip;
+      w.plane = pair_planes + v % p.tail_planes;
+      w.q0 = (p.n_qblk - 1 - v / p.tail_planes) * 256;
+    }
+    return bf16_geometry(p, w, false);
+  }
+  if (u >= p.n_tiles) return kTileEnd;
+  while (cur.s < p.nseq) {
+    const int sq = order ? static_cast<int>(order[cur.s]) : cur.s;
+    const int a = __ldg(p.cu_seqlens + sq), e = __ldg(p.cu_seqlens + sq + 1);
+    if (a < 0 || e < a || e > p.rows) {
+      if (threadIdx.x == 0) atomicOr(p.err, kDevErrBounds);
+      return kTileEnd;
+    }
+    const int nb = (e - a + 255) / 256;
+    const int npp = (nb + 1) / 2;
+    if (u < cur.cum + npp * p.planes) {
+      const int ak = __ldg(p.cu_seqlens_k + sq), ek = __ldg(p.cu_seqlens_k + sq + 1);
+      if (ak < 0 || ek < ak || ek > p.rows_k) {
+        if (threadIdx.x == 0) atomicOr(p.err, kDevErrBounds);
+        return kTileEnd;
+      }
+      const int r = u - cur.cum;
+      w.plane = r / npp;
+      const int pb = r - w.plane * npp;
+      const int heavy = nb - 1 - pb;
+      if (h) {
+        if (pb == heavy) return kTileSkip;
+        w.q0 = pb * 256;
+      } else {
+        w.q0 = heavy * 256;
+      }
+      w.row_base = a;
+      w.seq_len = e - a;
+      w.kv_base = ak;
+      w.kv_len = ek - ak;
+      return bf16_geometry(p, w, false);
+    }
+    cur.cum += npp * p.planes;
+    ++cur.s;
+  }
+  return kTileEnd;
+}
+
+// The producer's walk over the work tiles.
+struct TileWalk {
+  int k = 0;     // items (static schedule: iterations) taken so far
+  int u = 0;     // current item
+  int half = 2;  // next half of the current item (2: take a new item)
+  SeqCursor cur;
+};
+
+// Next work tile of this CTA, decoded by the TMA producer warp (a
+// warp-uniform call).  Static schedule: the next tile of the list.  Item
+// schedule: the halves of the current item, then a new item: the CTA's first
+// is blockIdx.x, every later one the next free position of the launch's
+// counter (past the first gridDim.x).  kTileSkip marks a half that does not
+// exist.
+__device__ __forceinline__ int bf16_take(const Bf16Params& p, const uint16_t* order,
+                                         TileWalk& src, WorkTile& w) {
+  if (p.sched == nullptr) return bf16_tile_static(p, src.k++, w);
+  if (src.half == 2) {
+    int u = static_cast<int>(blockIdx.x);
+    if (src.k > 0) {
+      unsigned int t = 0;
+      if ((threadIdx.x % 32) == 0) t = atomicAdd(p.sched, 1u);
+      u = static_cast<int>(gridDim.x + __shfl_sync(0xffffffffu, t, 0));
+    }
+    ++src.k;
+    src.u = u;
+    src.half = 0;
+  }
+  return bf16_item(p, order, src.u, src.half++, src.cur, w);
+}
+
+// The tiles the producer takes reach the MMA and softmax warps through a ring
+// of kItemRing slots in shared memory: a slot holds the tile (or the end of
+// the walk) as twelve 32-bit words, item_full[slot] completes when it is
+// written, item_empty[slot] when all nine readers have copied it.  Addresses
+// are 32-bit shared-memory addresses: the ring's first slot and the first
+// item_full barrier (the item_empty barriers follow them).
+constexpr uint32_t kItemSlotBytes = 48;
+
+// Producer: publish the n-th tile (step is kTileRun or kTileEnd).
+__device__ __forceinline__ bool bf16_publish(uint32_t ring, uint32_t full, int n, int step,
+                                             const WorkTile& w, const WaitCtl& ctl) {
+  const uint32_t slot = static_cast<uint32_t>(n % kItemRing);
+  const uint32_t lap = static_cast<uint32_t>(n / kItemRing);
+  const uint32_t empty = full + 8 * kItemRing;
+  if (lap > 0 && !__all_sync(0xffffffffu, mbar_wait_at(empty + 8 * slot, (lap - 1) & 1, ctl)))
+    return false;
+  if ((threadIdx.x % 32) == 0) {
+    const uint32_t a = ring + kItemSlotBytes * slot;
+    st_shared_v4(a, step, w.plane, w.row_base, w.seq_len);
+    st_shared_v4(a + 16, w.kv_base, w.kv_len, w.q0, w.has_q1 ? 1 : 0);
+    st_shared_v4(a + 32, w.n0, w.n1, 0, 0);
+    mbar_arrive_at(full + 8 * slot);  // release: the slot's contents are visible to its readers
+  }
+  __syncwarp();
+  return true;
+}
+
+// Reader (MMA or softmax warp, warp-uniform): the n-th tile; kTileEnd at the
+// end of the walk or when the CTA is aborting.
+__device__ __forceinline__ int bf16_read(uint32_t ring, uint32_t full, int n, WorkTile& w,
+                                         const WaitCtl& ctl) {
+  const uint32_t slot = static_cast<uint32_t>(n % kItemRing);
+  const uint32_t lap = static_cast<uint32_t>(n / kItemRing);
+  if (!__all_sync(0xffffffffu, mbar_wait_at(full + 8 * slot, lap & 1, ctl))) return kTileEnd;
+  const uint32_t a = ring + kItemSlotBytes * slot;
+  uint32_t r0[4], r1[4], r2[4];
+  ld_shared_v4(a, r0);
+  ld_shared_v4(a + 16, r1);
+  ld_shared_v4(a + 32, r2);
+  w.plane = static_cast<int>(r0[1]);
+  w.row_base = static_cast<int>(r0[2]);
+  w.seq_len = static_cast<int>(r0[3]);
+  w.kv_base = static_cast<int>(r1[0]);
+  w.kv_len = static_cast<int>(r1[1]);
+  w.q0 = static_cast<int>(r1[2]);
+  w.has_q1 = r1[3] != 0;
+  w.n0 = static_cast<int>(r2[0]);
+  w.n1 = static_cast<int>(r2[1]);
+  __syncwarp();
+  if ((threadIdx.x % 32) == 0) mbar_arrive_at(full + 8 * kItemRing + 8 * slot);
+  return static_cast<int>(r0[0]);
+}
+
+// A CTA is done with the launch's work counter; the last one resets it, so
+// that the next launch given the same counter starts from zero.
+__device__ __forceinline__ void sched_done(unsigned int* sched) {
+  __threadfence();
+  if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+    atomicExch(sched, 0u);
+    atomicExch(sched + 1, 0u);
+  }
 }
 
 // S = Q K^T for one 128x128 tile: D/16 MMAs of K=16.  q_desc/k_desc are the
@@ -331,6 +457,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* o_full = p_full + 2;     // [2]
   uint64_t* mma_done = o_full + 2;
   uint64_t* p_free = mma_done + 1;   // [2] (kSplitP: the P V of the last P is complete)
+  uint64_t* item_full = bars + C::ITEM_FULL_BAR;  // [kItemRing]
+  uint64_t* item_empty = bars + C::ITEM_EMPTY_BAR;  // [kItemRing]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -344,7 +472,12 @@ __global__ void __launch_bounds__(320, 1)
   {
     SeqCursor c0;
     WorkTile w0;
-    if (bf16_tile(p, order, 0, c0, w0) != kTileRun) return;  // uniform: no work for this CTA
+    const int first = p.sched ? bf16_item(p, order, static_cast<int>(blockIdx.x), 0, c0, w0)
+                              : bf16_tile_static(p, 0, w0);
+    if (first != kTileRun) {  // uniform: no work for this CTA
+      if (p.sched && threadIdx.x == 0) sched_done(p.sched);
+      return;
+    }
   }
 
   const int warp = threadIdx.x / 32;
@@ -364,6 +497,10 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(mma_done, 1);
+    for (int i = 0; i < kItemRing; ++i) {
+      mbar_init(&item_full[i], 1);
+      mbar_init(&item_empty[i], 9);  // the eight softmax warps and the MMA warp
+    }
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -377,6 +514,9 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
   const uint32_t smem_base = smem_u32(smem);
+  const uint32_t item_ring = smem_base + C::ITEM_OFF;
+  const uint32_t item_bar = smem_base + C::BAR_OFF + 8 * C::ITEM_FULL_BAR;
+  int n_tile = 0;  // work tiles read (MMA and softmax warps) or published (producer)
 
   if (warp < 8) {
     // ------------------------------------------------------------ softmax
@@ -390,10 +530,9 @@ __global__ void __launch_bounds__(320, 1)
     const float cl2 = p.scale_log2;
     const uint64_t c2 = f32x2(cl2, cl2);
     uint32_t n_s = 0, n_o = 0;  // s_full / o_full phases consumed so far
-    SeqCursor cur;
     WorkTile w;
-    for (int it = 0;; ++it) {
-      const int step = bf16_tile(p, order, it, cur, w);
+    for (;;) {
+      const int step = bf16_read(item_ring, item_bar, n_tile++, w, ctl);
       if (step == kTileEnd) break;
       if (step == kTileSkip || (ti == 1 && !w.has_q1)) continue;
       const int n_i = ti ? w.n1 : w.n0;
@@ -541,7 +680,6 @@ __global__ void __launch_bounds__(320, 1)
     uint32_t n_q[2] = {0, 0}, n_p[2] = {0, 0};
     int g = 0;  // ring position of the tile's K_0
     bool ok = true;
-    SeqCursor cur;
     WorkTile w;
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl));
@@ -549,8 +687,8 @@ __global__ void __launch_bounds__(320, 1)
     // abort-path test: mma_done completes only after this warp's own final
     // commit, so this wait runs out of budget and the whole CTA aborts
     if (p.stall && blockIdx.x == 0) ok = wait(mma_done, 0);
-    for (int it = 0; ok; ++it) {
-      const int step = bf16_tile(p, order, it, cur, w);
+    while (ok) {
+      const int step = bf16_read(item_ring, item_bar, n_tile++, w, ctl);
       if (step == kTileEnd) break;
       if (step == kTileSkip) continue;
       const int nmax = max(w.n0, w.n1);
@@ -643,7 +781,6 @@ __global__ void __launch_bounds__(320, 1)
     uint32_t n_q[2] = {0, 0};
     int g = 0;  // ring positions issued
     bool ok = true;
-    SeqCursor cur;
     WorkTile w;
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl));
@@ -661,10 +798,12 @@ __global__ void __launch_bounds__(320, 1)
       ++g;
       return true;
     };
-    for (int it = 0; ok; ++it) {
-      const int step = bf16_tile(p, order, it, cur, w);
-      if (step == kTileEnd) break;
+    TileWalk walk;
+    while (ok) {
+      const int step = bf16_take(p, order, walk, w);
       if (step == kTileSkip) continue;
+      ok = bf16_publish(item_ring, item_bar, n_tile++, step, w, ctl);
+      if (step == kTileEnd) break;
       const int nkv = 2 * max(w.n0, w.n1);
       // K_0 and V_0 first: their slots are freed by the previous tile alone
       const int head = min(2, nkv);
@@ -698,6 +837,7 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  if (p.sched && threadIdx.x == 0) sched_done(p.sched);
 }
 
 }  // namespace attn

@@ -257,8 +257,11 @@ def test_long_plane_sampled(N, D, causal):
 @pytest.mark.parametrize("N", [1280, 1100])
 @pytest.mark.parametrize("causal", [False, True])
 def test_many_planes_several_blocks_every_element(N, causal):
-    # 160 planes of 5 blocks of 256 rows: 480 mirror pairs over the persistent
-    # CTAs, several rounds in alternating direction, every plane compared in full
+    # 160 planes of 5 blocks of 256 rows over the 148 persistent CTAs, every
+    # plane compared in full.  Causal: 330 mirror pairs of 110 planes, then
+    # the 250 single blocks of the last 50, handed out by the launch's work
+    # counter; non-causal: 800 single blocks in static rounds, the last one
+    # split into query tiles
     from concurrent.futures import ThreadPoolExecutor
     from oracle.threads import blas_threads
     B, H, D = 4, 40, 128
