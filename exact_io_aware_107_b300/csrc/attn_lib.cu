@@ -23,14 +23,15 @@ namespace attn {
 
 __device__ unsigned int g_dev_error;
 
-// Work counters of the forward kernel's causal and packed schedules: a launch
-// takes the next of kSchedSlots slots (two words each, padded to 32 bytes),
-// which every launch leaves at zero when its last CTA ends.  Launches in
-// flight at the same time use different slots unless kSchedSlots of them are;
-// replays of one captured launch reuse its slot and must not overlap.
+// Work counters of the persistent kernels (the forward's causal and packed
+// schedules, the backward): a launch takes the next of kSchedSlots slots (two
+// words each, padded to 32 bytes), which every launch leaves at zero when its
+// last CTA ends.  Launches in flight at the same time use different slots
+// unless kSchedSlots of them are; replays of one captured launch reuse its
+// slot and must not overlap.
 constexpr int kSchedSlots = 256;
 constexpr int kSchedStride = 8;  // words per slot
-__device__ unsigned int g_fwd_sched[kSchedSlots * kSchedStride];
+__device__ unsigned int g_sched[kSchedSlots * kSchedStride];
 
 // Scratch of attn_decode_noalloc: the per-slice decode partials of one call
 // (see include/attn_b300.h).  Fixed size, one copy per device, shared by every
@@ -50,8 +51,8 @@ std::atomic<int> g_stall{0};
 struct DeviceState {
   int checked = 0;  // 0 unknown, 1 ok, -1 wrong arch
   unsigned int* err = nullptr;
-  unsigned int* sched = nullptr;             // g_fwd_sched on this device
-  std::atomic<unsigned int> sched_next{0};   // slot of the next forward launch
+  unsigned int* sched = nullptr;             // g_sched on this device
+  std::atomic<unsigned int> sched_next{0};   // slot of the next launch
   bool attrs_set = false;
   int sms = 0;
 };
@@ -162,6 +163,11 @@ __global__ void __launch_bounds__(256)
   if ((threadIdx.x & 31) == 0) atomicXor(out, acc);
 }
 
+// The work counter of the next persistent launch on this device.
+unsigned int* next_sched_slot(DeviceState* st) {
+  return st->sched + (st->sched_next.fetch_add(1) % kSchedSlots) * kSchedStride;
+}
+
 // Checks the current device once and fetches what the launches need.
 int prepare_device(DeviceState** out) {
   int dev = 0;
@@ -188,7 +194,7 @@ int prepare_device(DeviceState** out) {
       }
       st.err = static_cast<unsigned int*>(p);
       void* ps = nullptr;
-      if (cudaGetSymbolAddress(&ps, g_fwd_sched) != cudaSuccess || ps == nullptr) {
+      if (cudaGetSymbolAddress(&ps, g_sched) != cudaSuccess || ps == nullptr) {
         cudaGetLastError();
         return ATTN_ERR_LAUNCH;
       }
@@ -372,9 +378,7 @@ int fwd_16bit(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.timeout_ns = g_timeout_ns.load();
   p.err = st->err;
   // the causal and packed schedules hand out their items from a counter
-  p.sched = (cu_q || causal)
-                ? st->sched + (st->sched_next.fetch_add(1) % kSchedSlots) * kSchedStride
-                : nullptr;
+  p.sched = (cu_q || causal) ? next_sched_slot(st) : nullptr;
 
   const unsigned grid = static_cast<unsigned>(std::min<long long>(items, st->sms));
   if (D == 64) {
@@ -552,8 +556,11 @@ int bwd_16bit(const void* q, const void* k, const void* v, const void* o, const 
   p.rows_k = Nk;
   p.n_kblk = (Nk + 127) / 128;
   const long long tiles = Nk == 0 ? 0 : (cu_q ? (1LL * (Nk / 128 + B)) : 1LL * p.n_kblk);
-  const long long grid = tiles * planes;
-  if (grid > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  // persistent: one CTA per SM at most, taking the key tiles (work items)
+  // from the launch's counter, heaviest first
+  const long long items = tiles * planes;
+  if (items > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  const long long grid = std::min<long long>(items, st->sms);
   p.n_tiles = static_cast<int>(tiles);
   p.causal = causal ? 1 : 0;
   p.scale = scale;
@@ -561,6 +568,7 @@ int bwd_16bit(const void* q, const void* k, const void* v, const void* o, const 
   p.stall = g_stall.load();
   p.timeout_ns = g_timeout_ns.load();
   p.err = st->err;
+  p.sched = next_sched_slot(st);
   const unsigned g = static_cast<unsigned>(grid);
   if (D == 64) {
     if (f16)

@@ -275,7 +275,7 @@ __device__ __forceinline__ int bf16_item(const Bf16Params& p, const uint16_t* or
     const int sq = order ? static_cast<int>(order[cur.s]) : cur.s;
     const int a = __ldg(p.cu_seqlens + sq), e = __ldg(p.cu_seqlens + sq + 1);
     if (a < 0 || e < a || e > p.rows) {
-      if (threadIdx.x == 0) atomicOr(p.err, kDevErrBounds);
+      if ((threadIdx.x % 32) == 0) atomicOr(p.err, kDevErrBounds);
       return kTileEnd;
     }
     const int nb = (e - a + 255) / 256;
@@ -283,7 +283,7 @@ __device__ __forceinline__ int bf16_item(const Bf16Params& p, const uint16_t* or
     if (u < cur.cum + npp * p.planes) {
       const int ak = __ldg(p.cu_seqlens_k + sq), ek = __ldg(p.cu_seqlens_k + sq + 1);
       if (ak < 0 || ek < ak || ek > p.rows_k) {
-        if (threadIdx.x == 0) atomicOr(p.err, kDevErrBounds);
+        if ((threadIdx.x % 32) == 0) atomicOr(p.err, kDevErrBounds);
         return kTileEnd;
       }
       const int r = u - cur.cum;
@@ -326,14 +326,7 @@ __device__ __forceinline__ int bf16_take(const Bf16Params& p, const uint16_t* or
                                          TileWalk& src, WorkTile& w) {
   if (p.sched == nullptr) return bf16_tile_static(p, src.k++, w);
   if (src.half == 2) {
-    int u = static_cast<int>(blockIdx.x);
-    if (src.k > 0) {
-      unsigned int t = 0;
-      if ((threadIdx.x % 32) == 0) t = atomicAdd(p.sched, 1u);
-      u = static_cast<int>(gridDim.x + __shfl_sync(0xffffffffu, t, 0));
-    }
-    ++src.k;
-    src.u = u;
+    src.u = sched_take(p.sched, src.k++);
     src.half = 0;
   }
   return bf16_item(p, order, src.u, src.half++, src.cur, w);
@@ -368,6 +361,7 @@ __device__ __forceinline__ bool bf16_publish(uint32_t ring, uint32_t full, int n
 
 // Reader (MMA or softmax warp, warp-uniform): the n-th tile; kTileEnd at the
 // end of the walk or when the CTA is aborting.
+template <bool kRelease = true>
 __device__ __forceinline__ int bf16_read(uint32_t ring, uint32_t full, int n, WorkTile& w,
                                          const WaitCtl& ctl) {
   const uint32_t slot = static_cast<uint32_t>(n % kItemRing);
@@ -387,19 +381,31 @@ __device__ __forceinline__ int bf16_read(uint32_t ring, uint32_t full, int n, Wo
   w.has_q1 = r1[3] != 0;
   w.n0 = static_cast<int>(r2[0]);
   w.n1 = static_cast<int>(r2[1]);
-  __syncwarp();
-  if ((threadIdx.x % 32) == 0) mbar_arrive_at(full + 8 * kItemRing + 8 * slot);
+  if (kRelease) {
+    __syncwarp();
+    if ((threadIdx.x % 32) == 0) mbar_arrive_at(full + 8 * kItemRing + 8 * slot);
+  }
   return static_cast<int>(r0[0]);
 }
 
-// A CTA is done with the launch's work counter; the last one resets it, so
-// that the next launch given the same counter starts from zero.
-__device__ __forceinline__ void sched_done(unsigned int* sched) {
-  __threadfence();
-  if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
-    atomicExch(sched, 0u);
-    atomicExch(sched + 1, 0u);
-  }
+// A reader that keeps its slot until the end of the tile (the softmax warps,
+// whose registers are scarcest) reads the plane, first row and length of the
+// tile again from it when it writes O, instead of holding them in registers
+// through the key loop, and releases the slot when it takes the next tile.
+// Words of a slot: 0 step, 1 plane, 2 row_base, 3 seq_len, 4 kv_base,
+// 5 kv_len, 6 q0, 7 has_q1, 8 n0, 9 n1.
+__device__ __forceinline__ uint32_t bf16_slot_word(uint32_t ring, int n, int word) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];"
+               : "=r"(v)
+               : "r"(ring + kItemSlotBytes * static_cast<uint32_t>(n % kItemRing) + 4 * word)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void bf16_release(uint32_t full, int n) {
+  __syncwarp();
+  if ((threadIdx.x % 32) == 0)
+    mbar_arrive_at(full + 8 * kItemRing + 8 * static_cast<uint32_t>(n % kItemRing));
 }
 
 // S = Q K^T for one 128x128 tile: D/16 MMAs of K=16.  q_desc/k_desc are the
@@ -531,8 +537,9 @@ __global__ void __launch_bounds__(320, 1)
     const uint64_t c2 = f32x2(cl2, cl2);
     uint32_t n_s = 0, n_o = 0;  // s_full / o_full phases consumed so far
     WorkTile w;
-    for (;;) {
-      const int step = bf16_read(item_ring, item_bar, n_tile++, w, ctl);
+    for (;; ++n_tile) {
+      if (n_tile > 0) bf16_release(item_bar, n_tile - 1);
+      const int step = bf16_read<false>(item_ring, item_bar, n_tile, w, ctl);
       if (step == kTileEnd) break;
       if (step == kTileSkip || (ti == 1 && !w.has_q1)) continue;
       const int n_i = ti ? w.n1 : w.n0;
@@ -541,8 +548,9 @@ __global__ void __launch_bounds__(320, 1)
       const int off = w.kv_len - w.seq_len;         // causal alignment of queries to keys
       if (n_i == 0) {
         // every row of this tile sees no key
-        if (row < w.seq_len) {
-          const size_t grow = static_cast<size_t>(w.plane) * p.rows + w.row_base + row;
+        if (row < static_cast<int>(bf16_slot_word(item_ring, n_tile, 3))) {
+          const size_t grow = static_cast<size_t>(bf16_slot_word(item_ring, n_tile, 1)) * p.rows +
+                              bf16_slot_word(item_ring, n_tile, 2) + row;
           uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + grow * D);
 #pragma unroll
           for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
@@ -646,8 +654,9 @@ __global__ void __launch_bounds__(320, 1)
       if (!ok || !__all_sync(0xffffffffu, mbar_wait(&o_full[ti], n_o & 1, ctl))) break;
       ++n_o;
       tc_fence_after();
-      const bool valid = row < w.seq_len;
-      const size_t grow = static_cast<size_t>(w.plane) * p.rows + w.row_base + row;
+      const bool valid = row < static_cast<int>(bf16_slot_word(item_ring, n_tile, 3));
+      const size_t grow = static_cast<size_t>(bf16_slot_word(item_ring, n_tile, 1)) * p.rows +
+                          bf16_slot_word(item_ring, n_tile, 2) + row;
       // l == 0 only for a row that saw no allowed key: O = 0, LSE = -inf
       const float inv_l = (l > 0.f) ? 1.f / l_o : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + grow * D);

@@ -109,6 +109,32 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 }
 
 // ----------------------------------------------------------------------------
+// Work counters of the persistent kernels
+// ----------------------------------------------------------------------------
+
+// The next work item of a persistent CTA (a warp-uniform call): the CTA's
+// first is blockIdx.x, every later one the next free position of the launch's
+// counter past the first gridDim.x, so the items go in list order to
+// whichever CTA asks first.
+__device__ __forceinline__ int sched_take(unsigned int* sched, int taken) {
+  if (taken == 0) return static_cast<int>(blockIdx.x);
+  unsigned int t = 0;
+  if ((threadIdx.x % 32) == 0) t = atomicAdd(sched, 1u);
+  return static_cast<int>(gridDim.x + __shfl_sync(0xffffffffu, t, 0));
+}
+
+// A CTA is done with the launch's work counter (two words: next item, CTAs
+// finished); the last one resets it, so that the next launch given the same
+// counter starts from zero.
+__device__ __forceinline__ void sched_done(unsigned int* sched) {
+  __threadfence();
+  if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+    atomicExch(sched, 0u);
+    atomicExch(sched + 1, 0u);
+  }
+}
+
+// ----------------------------------------------------------------------------
 // TMA (tiled tensor copies global -> shared, completion counted on an mbarrier)
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {

@@ -1,13 +1,15 @@
-"""The forward's work counter.
+"""The work counters of the persistent kernels.
 
-The causal and the packed layouts hand their work items (pairs of 256-row
-blocks, then single blocks) to whichever persistent CTA asks first, from a
-counter in device memory that the last CTA of each launch resets to zero.
-What must hold: every call covers every query row, whatever launches came
-before it on the same counter; repeated calls, CUDA-graph replays and more
-launches than the library has counters give the same bits as one call; and
-that call matches the oracle in every element.  Outputs are filled with NaN
-before every call, so a skipped item cannot pass.
+The forward's causal and packed layouts hand their work items (pairs of
+256-row blocks, then single blocks) to whichever persistent CTA asks first,
+and so does the backward with its key tiles, from a counter in device memory
+that the last CTA of each launch resets to zero.  What must hold: every call
+covers every query row (forward) and every key row (backward), whatever
+launches came before it on the same counter; repeated calls, CUDA-graph
+replays and more launches than the library has counters give the same bits
+as one call (dQ of the backward, summed over key tiles in a free order, up to
+fp32 reassociation); and that call matches the oracle in every element.
+Outputs are filled with NaN before every call, so a skipped item cannot pass.
 """
 
 from concurrent.futures import ThreadPoolExecutor
@@ -17,7 +19,7 @@ import pytest
 
 import oracle
 from exact_io_aware_107_b300 import workloads as W
-from gpu_util import BF16_TOL_LSE, BF16_TOL_O, max_err
+from gpu_util import BF16_TOL_LSE, BF16_TOL_O, UNIT, bwd_bound_plane, max_err, run_cuda_bwd
 
 pytestmark = pytest.mark.gpu
 
@@ -162,3 +164,95 @@ def test_more_launches_than_counters():
     assert device_error() == 0
     eo, el = _oracle_errors(w, x, ref_o, ref_lse)
     assert eo <= BF16_TOL_O and el <= BF16_TOL_LSE, (eo, el)
+
+
+# ---------------------------------------------------------------- backward
+
+def _dout_like(q, seed):
+    import torch
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    return torch.randn(q.shape, generator=g).to(q.dtype)
+
+
+@pytest.mark.parametrize("causal,D", [(True, 128), (False, 64)])
+def test_backward_several_key_tiles_per_cta_every_plane(causal, D):
+    # 80 planes of 10 key tiles: 800 work items over the persistent CTAs, so
+    # each CTA runs five or six key tiles back to back (the phases of every
+    # barrier carried from one key tile to the next); every plane is compared
+    # with the oracle's gradient within the error bound
+    B, H, N = 4, 20, 1280
+    w = W.custom("bf16", B=B, H=H, N=N, D=D, causal=causal, seed=90 + D)
+    x = W.generate(w)
+    do = _dout_like(x["q"], 91)
+    dq, dk, dv = run_cuda_bwd(x["q"], x["k"], x["v"], do, causal, w.scale)
+    f = W.as_f64
+    q, k, v, g = f(x["q"]), f(x["k"]), f(x["v"]), f(do)
+    u = UNIT["bf16"]
+
+    def one(bh):
+        b, h = bh
+        (rq, rk, rv), (bq, bk, bv) = bwd_bound_plane(q[b, h], k[b, h], v[b, h], g[b, h], w.scale,
+                                                     causal, u)
+        return max(float((np.abs(dq[b, h] - rq) - bq).max()),
+                   float((np.abs(dk[b, h] - rk) - bk).max()),
+                   float((np.abs(dv[b, h] - rv) - bv).max()))
+
+    from oracle.threads import blas_threads
+    with blas_threads(1):
+        with ThreadPoolExecutor(max_workers=8) as ex:
+            excess = list(ex.map(one, [(b, h) for b in range(B) for h in range(H)]))
+    assert max(excess) <= 0, max(excess)
+
+
+def test_backward_more_launches_than_counters():
+    # 300 backward calls on two streams: every call finds its counter at zero,
+    # dK and dV equal the first call's bit for bit, dQ up to reassociation
+    import torch
+    from exact_io_aware_107_b300 import attention_backward, attention_forward, device_error
+    w = W.custom("bf16", B=2, H=3, N=700, D=128, causal=True, seed=92)
+    x = W.generate(w)
+    q, k, v = (t.cuda() for t in (x["q"], x["k"], x["v"]))
+    do = _dout_like(x["q"], 93).cuda()
+    o, lse = attention_forward(q, k, v, causal=True)
+    ref = attention_backward(q, k, v, o, lse, do, causal=True)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [tuple(torch.empty_like(t) for t in ref) for _ in range(4)]
+    wss = [None, None]
+    for i in range(300):
+        s = streams[i % 2]
+        dq, dk, dv = outs[i % 4]
+        with torch.cuda.stream(s):
+            for t in (dq, dk, dv):
+                t.fill_(float("nan"))
+            attention_backward(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv, stream=s)
+        if i % 4 == 3:
+            torch.cuda.synchronize()
+            for dq, dk, dv in outs:
+                assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2]), i
+                assert (dq.float() - ref[0].float()).abs().max() <= 2.0 ** -7 * max(
+                    1.0, ref[0].float().abs().max().item()), i
+    assert device_error() == 0
+
+
+def test_malformed_offsets_late_in_the_list_are_reported():
+    # the bad offsets come after 199 good sequences, so only a work item taken
+    # late (decoded by the producer warp alone, not at a CTA's start) meets them
+    import torch
+    from exact_io_aware_107_b300 import (_binding, attention_backward, attention_forward,
+                                         device_error)
+    n = 200 * 256
+    x = W.generate(W.custom("bf16", B=1, H=1, N=n, D=128, seed=94))
+    q, k, v = (t[0].contiguous().cuda() for t in (x["q"], x["k"], x["v"]))
+    cu = torch.arange(0, n + 1, 256, dtype=torch.int32)
+    cu[-1] = cu[-2] - 10  # decreasing: the last sequence is malformed
+    cu = cu.cuda()
+    assert device_error() == 0
+    for causal in (True, False):
+        o, lse = attention_forward(q, k, v, causal=causal, cu_seqlens=cu)
+        assert device_error() == _binding.ATTN_ERR_BOUNDS
+        o = torch.zeros_like(q)
+        lse = torch.zeros(q.shape[:-1], dtype=torch.float32, device="cuda")
+        attention_backward(q, k, v, o, lse, q, causal=causal, cu_seqlens=cu)
+        assert device_error() == _binding.ATTN_ERR_BOUNDS
+    assert device_error() == 0
