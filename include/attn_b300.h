@@ -35,6 +35,14 @@
  * returns.  The host never reads cu_seqlens, so the grid is sized from N and
  * B and surplus CTAs exit at once.
  *
+ * Work counters: the 16-bit forward (causal or packed) and the backward run
+ * persistent CTAs that take their work items from a counter in the library's
+ * static device memory (one of 256 per device, a new one per call, left at
+ * zero by the last CTA of the launch).  Calls in flight at the same time get
+ * different counters unless 256 of them are; the replays of one CUDA-graph
+ * capture of a call reuse that call's counter, so they must not run
+ * concurrently with each other (replays in stream order are fine).
+ *
  * Errors: argument problems are reported synchronously by the return value
  * and nothing is launched.  Problems only the device can see (a wait that ran
  * out of time, cu_seqlens entries outside [0, N] or decreasing) set bits in a
