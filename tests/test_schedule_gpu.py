@@ -256,3 +256,35 @@ def test_malformed_offsets_late_in_the_list_are_reported():
         attention_backward(q, k, v, o, lse, q, causal=causal, cu_seqlens=cu)
         assert device_error() == _binding.ATTN_ERR_BOUNDS
     assert device_error() == 0
+
+
+@pytest.mark.parametrize("dtype,causal", [("bf16", True), ("f16", False)])
+def test_backward_packed_many_sequences_every_sequence(dtype, causal):
+    # 40 packed sequences of 1..700 rows over 4 heads: several hundred key
+    # tiles, so each persistent CTA walks several sequences' key tiles; every
+    # (sequence, head) is compared with the oracle's gradient within the bound
+    rng = np.random.default_rng(95)
+    lens = [int(x) for x in rng.integers(1, 701, 40)]
+    w = W.custom(dtype, H=4, D=128, causal=causal, seed=96, varlen=lens)
+    x = W.generate(w)
+    do = _dout_like(x["q"], 97)
+    dq, dk, dv = run_cuda_bwd(x["q"], x["k"], x["v"], do, causal, w.scale, x["cu_seqlens"])
+    f = W.as_f64
+    q, k, v, g = f(x["q"]), f(x["k"]), f(x["v"]), f(do)
+    cu = np.asarray(x["cu_seqlens"])
+    u = UNIT[dtype]
+
+    def one(hs):
+        h, s = hs
+        a, e = int(cu[s]), int(cu[s + 1])
+        (rq, rk, rv), (bq, bk, bv) = bwd_bound_plane(q[h, a:e], k[h, a:e], v[h, a:e], g[h, a:e],
+                                                     w.scale, causal, u)
+        return max(float((np.abs(dq[h, a:e] - rq) - bq).max()),
+                   float((np.abs(dk[h, a:e] - rk) - bk).max()),
+                   float((np.abs(dv[h, a:e] - rv) - bv).max()))
+
+    from oracle.threads import blas_threads
+    with blas_threads(1):
+        with ThreadPoolExecutor(max_workers=8) as ex:
+            excess = list(ex.map(one, [(h, s) for h in range(w.H) for s in range(len(lens))]))
+    assert max(excess) <= 0, max(excess)
